@@ -1,0 +1,336 @@
+"""Pins of the CPU oracle against facts fixed outside it (closed forms, library
+routines, brute force, invariants).  CPU only.
+
+The method follows "RetroInfer: A Vector Storage Engine for Scalable
+Long-Context LLM Inference" (technical summaries §2.A / §2.a and §3).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import wave_index as wi
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ---------------------------------------------------------------- helpers
+
+def sdpa64(q, K, V, scale):
+    """Softmax attention of one query by torch's library routine, float64."""
+    qt = torch.from_numpy(np.asarray(q, np.float64)).view(1, 1, 1, -1)
+    Kt = torch.from_numpy(np.asarray(K, np.float64)).view(1, 1, K.shape[0], -1)
+    Vt = torch.from_numpy(np.asarray(V, np.float64)).view(1, 1, V.shape[0], -1)
+    out = torch.nn.functional.scaled_dot_product_attention(qt, Kt, Vt, scale=scale)
+    lse = torch.logsumexp(scale * (Kt[0, 0] @ qt[0, 0, 0]), dim=0)
+    return out.view(-1).numpy(), float(lse)
+
+
+def bf16_vals(rng, shape, scale=1.0):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+
+
+def vsum_atol(idx):
+    """Bound on the output error caused by storing value sums in float32: each
+    estimated cluster weighs in with e^{s_c-M}/L <= 1/n_c, and the weights'
+    masses sum to at most 1."""
+    n = np.maximum(idx["size"], 1)[:, None]
+    return 2.0 ** -23 * float(np.max(np.abs(idx["value_sum"]) / n, initial=0.0)) + 1e-13
+
+
+def small_case(seed=0, N=700, d=128, sink=4, window=32, seg_len=256, k=16, iters=3,
+               planted=6):
+    rng = np.random.default_rng(seed)
+    means = rng.standard_normal((planted, d))
+    lab = rng.integers(0, planted, N)
+    K = bf16_vals(rng, (N, d), 0.4) + torch.from_numpy(means[lab]).to(torch.bfloat16).double().numpy()
+    K = torch.from_numpy(K).to(torch.bfloat16).double().numpy()
+    V = bf16_vals(rng, (N, d))
+    q = bf16_vals(rng, (d,))
+    idx = wi.build_index_head(K, V, sink, window, seg_len, k, iters)
+    return K, V, q, idx
+
+
+# ---------------------------------------------------------------- number format
+
+def test_bf16_round_matches_torch_cast():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-3).astype(np.float32),
+        # exact halfway cases between two bf16 neighbours: low 16 bits = 0x8000
+        ((rng.integers(0x3F000000, 0x40800000, 4000, dtype=np.uint32) & 0xFFFF0000) | 0x8000)
+        .view(np.float32),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(wi.bf16_round(x.astype(np.float64)), ref)
+
+
+def test_bf16_round_fp64_is_nearest_ties_even():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(20000)
+    y = wi.bf16_round(x)
+    # neighbours: y is a bf16 value; its distance to x is at most half an ulp
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(y))) - 7)
+    assert np.all(np.abs(x - y) <= ulp / 2 + 1e-300)
+    yb = torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(y, yb)  # y is representable in bf16
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_hand_derived():
+    g = json.load(open(os.path.join(HERE, "golden", "worked_example_2d.json")))
+    K = np.array(g["K"], np.float64)
+    V = np.array(g["V"], np.float64)
+    q = np.array(g["q"], np.float64)
+    idx = wi.build_index_head(K, V, g["sink"], g["window"], g["seg_len"], g["k_per_seg"],
+                              g["iters"])
+    for key, val in g["expect_index"].items():
+        np.testing.assert_array_equal(idx[key], np.array(val), err_msg=key)
+    for r, e in g["expect_decode"].items():
+        res = wi.decode_head(q, K, V, idx, g["sink"], g["window"], int(r), g["scale"])
+        np.testing.assert_allclose(res["out"], e["out"], rtol=1e-13)
+        assert abs(res["lse"] - e["lse"]) < 1e-13
+        np.testing.assert_array_equal(res["selected"], e["selected"])
+        if "token_w" in e:
+            np.testing.assert_allclose(res["token_w"], e["token_w"], rtol=1e-13)
+            np.testing.assert_allclose(res["est_w"], e["est_w"], rtol=1e-13)
+
+
+# ---------------------------------------------------------------- decode pins
+
+@pytest.mark.parametrize("d", [4, 128])
+def test_full_budget_equals_full_attention(d):
+    K, V, q, idx = small_case(seed=3, d=d)
+    scale = 1 / math.sqrt(d)
+    C = idx["n_clusters"]
+    for r in (int((idx["size"] > 0).sum()), C, C + 7):
+        res = wi.decode_head(q, K, V, idx, 4, 32, r, scale)
+        out, lse = sdpa64(q, K, V, scale)
+        np.testing.assert_allclose(res["out"], out, rtol=1e-11, atol=1e-13)
+        assert abs(res["lse"] - lse) < 1e-11
+
+
+def test_singleton_clusters_make_estimation_exact():
+    # k_per_seg >= tokens per segment with strided init: every token seeds its
+    # own centroid and is its own (singleton) cluster.
+    rng = np.random.default_rng(4)
+    N, d, seg = 300, 32, 64
+    K = bf16_vals(rng, (N, d))
+    V = bf16_vals(rng, (N, d))
+    q = bf16_vals(rng, (d,))
+    idx = wi.build_index_head(K, V, 3, 10, seg, seg, 2)
+    assert set(np.unique(idx["size"])) <= {0, 1}
+    out, lse = sdpa64(q, K, V, 0.3)
+    for r in (0, 1, 17, 1000):
+        res = wi.decode_head(q, K, V, idx, 3, 10, r, 0.3)
+        np.testing.assert_allclose(res["out"], out, rtol=1e-11, atol=1e-13)
+        assert abs(res["lse"] - lse) < 1e-11
+
+
+def test_zero_query_gives_mean_of_values():
+    K, V, q, idx = small_case(seed=5)
+    N = K.shape[0]
+    for r in (0, 3, 10 ** 6):
+        res = wi.decode_head(np.zeros_like(q), K, V, idx, 4, 32, r, 0.1)
+        np.testing.assert_allclose(res["out"], V.mean(axis=0), rtol=1e-11, atol=vsum_atol(idx))
+        assert abs(res["lse"] - math.log(N)) < 1e-12
+
+
+def test_tripartite_equals_attention_over_surrogate_keys():
+    # Characterisation of the estimation zone: every member of an estimated
+    # cluster takes its cluster's mean key, and softmax attention over that
+    # modified key set (torch SDPA) must equal the tripartite output.
+    K, V, q, idx = small_case(seed=6, d=64)
+    scale = 0.125
+    C = idx["n_clusters"]
+    for r in (0, 1, 5, 12):
+        res = wi.decode_head(q, K, V, idx, 4, 32, r, scale)
+        Ks = K.copy()
+        for c in range(C):
+            if c in set(res["selected"].tolist()):
+                continue
+            mem = idx["perm"][idx["offset"][c]:idx["offset"][c + 1]]
+            Ks[mem] = idx["centroid_key"][c]
+        out, lse = sdpa64(q, Ks, V, scale)
+        np.testing.assert_allclose(res["out"], out, rtol=1e-10, atol=vsum_atol(idx))
+        assert abs(res["lse"] - lse) < 1e-10
+
+
+def test_weights_sum_to_one():
+    K, V, q, idx = small_case(seed=7)
+    for r in (0, 2, 9):
+        res = wi.decode_head(q * 3, K, V, idx, 4, 32, r, 1 / math.sqrt(128))
+        assert abs(res["token_w"].sum() + res["est_w"].sum() - 1.0) < 1e-12
+        # out is the weighted combination
+        num = res["token_w"] @ V[res["token_pos"]]
+        num += (res["est_w"] / idx["size"][res["est_ids"]]) @ idx["value_sum"][res["est_ids"]]
+        np.testing.assert_allclose(num, res["out"], rtol=1e-11, atol=1e-13)
+
+
+def test_bruteforce_full_attention_loops():
+    rng = np.random.default_rng(8)
+    for d in (4, 128):
+        N = 64
+        K = bf16_vals(rng, (N, d))
+        V = bf16_vals(rng, (N, d))
+        q = bf16_vals(rng, (d,))
+        idx = wi.build_index_head(K, V, 2, 5, 32, 4, 2)
+        scale = 1 / math.sqrt(d)
+        res = wi.decode_head(q, K, V, idx, 2, 5, 100, scale)
+        # brute force with Python loops
+        logits = [scale * sum(q[j] * K[i, j] for j in range(d)) for i in range(N)]
+        mx = max(logits)
+        w = [math.exp(x - mx) for x in logits]
+        tot = sum(w)
+        ref = [sum(w[i] * V[i, j] for i in range(N)) / tot for j in range(d)]
+        np.testing.assert_allclose(res["out"], ref, rtol=1e-11, atol=1e-13)
+        assert abs(res["lse"] - (mx + math.log(tot))) < 1e-11
+
+
+def test_degenerate_zones():
+    K, V, q, idx = small_case(seed=9, N=300)
+    N = K.shape[0]
+    # window covering everything after the sinks: no index, pure exact attention
+    idx2 = wi.build_index_head(K, V, 4, N - 4, 256, 16, 2)
+    assert idx2["size"].sum() == 0 and idx2["perm"].size == 0
+    res = wi.decode_head(q, K, V, idx2, 4, N - 4, 5, 0.2)
+    out, lse = sdpa64(q, K, V, 0.2)
+    np.testing.assert_allclose(res["out"], out, rtol=1e-11, atol=1e-13)
+    # no steady zone, no budget: estimation only
+    idx3 = wi.build_index_head(K, V, 0, 0, 128, 8, 2)
+    res = wi.decode_head(q, K, V, idx3, 0, 0, 0, 0.2)
+    assert res["token_pos"].size == 0
+    assert abs(res["est_w"].sum() - 1) < 1e-12
+
+
+def test_selection_order_and_ties():
+    s = np.array([1.0, 3.0, 3.0, -np.inf, 2.0, 3.0, 0.5])
+    # brute force: sort (score desc, id asc) by Python's sort
+    cand = sorted([(-s[c], c) for c in range(len(s)) if np.isfinite(s[c])])
+    for r in range(0, 9):
+        ref = sorted(c for _, c in cand[:r])
+        np.testing.assert_array_equal(wi.select_clusters(s, r), ref)
+    assert list(wi.select_clusters(s, 2)) == [1, 2]
+
+
+# ---------------------------------------------------------------- build pins
+
+def test_segments_hand_case():
+    segs = wi.segment_positions(N=20, sink=3, window=4, seg_len=8)
+    assert [list(x) for x in segs] == [list(range(3, 8)), list(range(8, 16)), []]
+    segs = wi.segment_positions(N=20, sink=0, window=0, seg_len=32)
+    assert [list(x) for x in segs] == [list(range(20))]
+
+
+def test_init_strided_hand_case():
+    # m = 10 keys along distinct axes; k = 4 picks floor(j*10/4) = 0, 2, 5, 7
+    keys = np.eye(10) * 3.0
+    mu = wi.kmeans_init(keys, 4)
+    np.testing.assert_array_equal(mu, np.eye(10)[[0, 2, 5, 7]])
+    assert np.all(wi.kmeans_init(np.zeros((0, 5)), 3) == 0)
+
+
+def test_assign_bruteforce_loops():
+    rng = np.random.default_rng(10)
+    for d in (4, 128):
+        keys = bf16_vals(rng, (50, d))
+        mu = wi.bf16_round(rng.standard_normal((9, d)))
+        mu[5] = mu[2]  # exact tie -> the lower index wins
+        a, cos = wi.kmeans_assign(keys, mu)
+        for i in range(50):
+            dots = [sum(keys[i, t] * mu[j, t] for t in range(d)) for j in range(9)]
+            best = 0
+            for j in range(1, 9):
+                if dots[j] > dots[best]:
+                    best = j
+            assert a[i] == best
+            assert best != 5
+            nrm = math.sqrt(sum(keys[i, t] ** 2 for t in range(d)))
+            assert abs(cos[i, best] - dots[best] / nrm) < 1e-12
+
+
+def test_update_maximises_cosine_sum():
+    rng = np.random.default_rng(11)
+    d = 16
+    keys = bf16_vals(rng, (80, d))
+    mu0 = wi.bf16_round(rng.standard_normal((5, d)))
+    a, _ = wi.kmeans_assign(keys, mu0)
+    mu, mu_exact = wi.kmeans_update(keys, a, mu0)
+    unit = keys / np.linalg.norm(keys, axis=1, keepdims=True)
+    for j in range(5):
+        mem = unit[a == j]
+        if len(mem) == 0:
+            np.testing.assert_array_equal(mu[j], mu0[j])
+            continue
+        best = (mem @ mu_exact[j]).sum()
+        assert abs(np.linalg.norm(mu_exact[j]) - 1) < 1e-12
+        for _ in range(200):  # no unit vector does better (Cauchy-Schwarz)
+            u = rng.standard_normal(d)
+            u /= np.linalg.norm(u)
+            assert (mem @ u).sum() <= best + 1e-12
+        # the stored centroid is the bf16 rounding of the exact one
+        assert np.all(np.abs(mu[j] - mu_exact[j]) <= 2.0 ** -8 * np.abs(mu_exact[j]) + 1e-300)
+
+
+def test_assignment_step_never_lowers_objective():
+    rng = np.random.default_rng(12)
+    keys = bf16_vals(rng, (400, 32))
+    a, mu, hist = wi.kmeans_segment(keys, 12, 6, trace=True)
+    unit = keys / np.linalg.norm(keys, axis=1, keepdims=True)
+    prev_a = None
+    for mu_in, a_t, mu_out in hist:
+        obj = (unit * mu_in[a_t]).sum()
+        if prev_a is not None:
+            assert obj >= (unit * mu_in[prev_a]).sum() - 1e-12
+        prev_a = a_t
+    np.testing.assert_array_equal(a, hist[-1][1])
+    np.testing.assert_array_equal(mu, hist[-1][2])
+
+
+def test_planted_clusters_recovered():
+    # Blocks of tokens around well separated directions, laid out in position
+    # order: strided init seeds one centroid per block, and the build must
+    # return exactly the planted partition with its block statistics.
+    rng = np.random.default_rng(13)
+    k, blk, d, sink, window = 8, 20, 64, 2, 6
+    dirs = np.linalg.qr(rng.standard_normal((d, d)))[0][:k] * 5
+    lab = np.repeat(np.arange(k), blk)
+    keys = torch.from_numpy(dirs[lab] + 0.05 * rng.standard_normal((k * blk, d))).to(
+        torch.bfloat16).double().numpy()
+    N = sink + k * blk + window
+    K = np.concatenate([bf16_vals(rng, (sink, d)), keys, bf16_vals(rng, (window, d))])
+    V = bf16_vals(rng, (N, d))
+    idx = wi.build_index_head(K, V, sink, window, 1 << 20, k, 5)
+    np.testing.assert_array_equal(idx["assign"][sink:N - window], lab)
+    np.testing.assert_array_equal(idx["size"], np.full(k, blk))
+    for c in range(k):
+        rows = sink + np.arange(c * blk, (c + 1) * blk)
+        np.testing.assert_allclose(idx["centroid_key"][c], np.mean(K[rows], axis=0), rtol=1e-6,
+                                   atol=1e-6)
+        np.testing.assert_allclose(idx["value_sum"][c], np.sum(V[rows], axis=0), rtol=1e-6,
+                                   atol=1e-6)
+
+
+def test_statistics_invariants_and_stable_order():
+    K, V, q, idx = small_case(seed=14, N=900, seg_len=200, k=10)
+    N = K.shape[0]
+    P = np.arange(4, N - 32)
+    assert idx["size"].sum() == len(P)
+    assert sorted(idx["perm"].tolist()) == P.tolist()
+    np.testing.assert_array_equal(idx["offset"][1:], np.cumsum(idx["size"]))
+    # brute-force stable sort by (cluster, position)
+    ref = sorted(P.tolist(), key=lambda p: (idx["assign"][p], p))
+    np.testing.assert_array_equal(idx["perm"], ref)
+    np.testing.assert_array_equal(idx["k_sorted"], K[idx["perm"]])
+    np.testing.assert_array_equal(idx["v_sorted"], V[idx["perm"]])
+    # clusters never cross their segment
+    for p in P:
+        assert idx["assign"][p] // 10 == p // 200
+    assert np.all(idx["assign"][:4] == -1) and np.all(idx["assign"][N - 32:] == -1)
