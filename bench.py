@@ -1,0 +1,493 @@
+"""Benchmark of wave-index tripartite decode attention on one B300 (or N
+replicas, one per GPU, under torchrun).
+
+One timed step = one decode query batch through every decode row of the hot
+path (cluster scoring, top-r selection, steady + retrieval attention with the
+estimation zone, log-sum-exp merge) against an index built on the GPU in the
+same run.  The index build (segmented spherical k-means + finalize) is timed
+in the same run and reported under "build"; "full_pass_ms" is one pass of
+every row (build + decode) for one batch.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead (the reference arm), on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attention queries/sec/layer at 128K ctx; achieved HBM GB/s vs 8 TB/s"
+UNIT = "queries/s/layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="wi", choices=["wi", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_128k_b1")
+    ap.add_argument("--budget-frac", type=float, default=None,
+                    help="retrieval budget as a fraction of clusters (default: workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-build-timing", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=1)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# roofline bookkeeping
+# ----------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("wi_decode.cu", "wi_device.cuh", "wi_internal.h", "wi_assign.cu", "wi_build.cu"):
+        with open(os.path.join(ROOT, "cluster_indexed_sparse_wi_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def retrieved_unique_bytes(topk, size, G):
+    """Bytes of K and V rows of the retrieved clusters, counted once per
+    (sequence, KV head, cluster) over the query heads of a group."""
+    import torch
+    B, Hq, r = topk.shape
+    Hkv = Hq // G
+    ids = topk.view(B, Hkv, G * r).long()
+    total = 0
+    for b in range(B):
+        for g in range(Hkv):
+            u = torch.unique(ids[b, g])
+            u = u[u >= 0]
+            total += int(size[b, g][u].sum().item())
+    return total * 128 * 2 * 2
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ----------------------------------------------------------------------------
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        return 1
+
+
+def oracle_decode_sample(w, g_np, index_np, r, seconds, heads_of_group=0):
+    """Times the oracle decode of the query heads of KV head `heads_of_group`
+    of sequence 0, repeated until `seconds` of CPU work; returns
+    (queries/s/layer, sample description, per-step seconds list)."""
+    from oracle import wave_index as wi
+    G = w.Hq // w.Hkv
+    gsel = heads_of_group
+    Kf = wi.bf16_bits_to_f64(g_np["K"][0, gsel])
+    Vf = wi.bf16_bits_to_f64(g_np["V"][0, gsel])
+    qf = wi.bf16_bits_to_f64(g_np["q"][0])
+    hi = {k: index_np[k] for k in ("size", "centroid_key", "value_sum", "perm", "offset")}
+    scale = 1.0 / math.sqrt(w.d)
+    times = []
+    t_end = time.perf_counter() + seconds
+    while True:
+        t0 = time.perf_counter()
+        for h in range(gsel * G, gsel * G + G):
+            wi.decode_head(qf[h], Kf, Vf, hi, w.sink, w.window, r, scale)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end:
+            break
+    per_query = statistics.mean(times) * (w.Hq / G)  # all Hq heads of one query
+    desc = ("oracle decode of the %d query heads of KV head %d of one sequence (of %d), "
+            "%d repetitions, scaled to all %d heads" % (G, gsel, w.Hq, len(times), w.Hq))
+    return 1.0 / per_query, desc, times
+
+
+def oracle_index_for_head(w, g_np, b=0, g=0):
+    from oracle import wave_index as wi
+    Kf = wi.bf16_bits_to_f64(g_np["K"][b, g])
+    Vf = wi.bf16_bits_to_f64(g_np["V"][b, g])
+    return wi.build_index_head(Kf, Vf, w.sink, w.window, w.seg_len, w.k_per_seg, w.iters)
+
+
+def run_reference(args, w, r):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import generate
+    t0 = time.perf_counter()
+    g_np = generate(w, batches=[0])
+    t_gen = time.perf_counter() - t0
+    idx = oracle_index_for_head(w, g_np)  # setup, untimed
+    from oracle import wave_index as wi
+    G = w.Hq // w.Hkv
+    Kf = wi.bf16_bits_to_f64(g_np["K"][0, 0])
+    Vf = wi.bf16_bits_to_f64(g_np["V"][0, 0])
+    qf = wi.bf16_bits_to_f64(g_np["q"][0])
+    scale = 1.0 / math.sqrt(w.d)
+
+    def step():
+        for h in range(G):
+            wi.decode_head(qf[h], Kf, Vf, idx, w.sink, w.window, r, scale)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    per_query = statistics.mean(times) * (w.Hq / G)
+    value = 1.0 / per_query
+    cores = blas_threads()
+    sample = ("each step: oracle decode of the %d query heads of KV head 0 of sequence 0 "
+              "(index of that head built by the oracle, untimed); value scaled to all %d heads"
+              % (G, w.Hq))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, r),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+        "setup_seconds": {"generate": t_gen},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, r):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+            "clusters_per_head": w.n_clusters, "seg_len": w.seg_len, "k_per_seg": w.k_per_seg,
+            "kmeans_iters": w.iters, "sink": w.sink, "window": w.window, "r": r,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "step": "decode (score, select, attend+estimate, merge) over an index built in the "
+                    "same run; build timed separately under 'build'"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def main():
+    args = parse()
+    from workloads import WORKLOADS, generate, retrieval_budget
+    w = WORKLOADS[args.workload]
+    r = retrieval_budget(w, args.budget_frac) if args.budget_frac else w.r
+    if args.impl == "reference":
+        return run_reference(args, w, r)
+
+    import torch
+    import torch.distributed as dist
+    import cluster_indexed_sparse_wi_b300 as wl
+    from cluster_indexed_sparse_wi_b300 import _lib
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk, pk_kind = peaks()
+
+    # per-rank replica: own sequences (weak scaling), no data-path collective
+    t0 = time.perf_counter()
+    wr = w if rank == 0 else w.replace(seeds=tuple(s + 100003 * rank for s in w.seeds))
+    g_np = generate(wr)
+    t_gen = time.perf_counter() - t0
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    K, V, q = up(g_np["K"]), up(g_np["V"]), up(g_np["q"])
+    cfg = wl.IndexConfig(w.B, w.Hkv, w.N, w.sink, w.window, w.seg_len, w.k_per_seg, w.iters)
+    ix = wl.WaveIndex(cfg, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- build (rows a1-a4), timed on its own
+    ix.build(K, V)
+    torch.cuda.synchronize()
+    assert ix.status() == 0
+    build = None
+    if not args.no_build_timing:
+        bt = []
+        for _ in range(3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ix.build(K, V)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            bt.append(e0.elapsed_time(e1))
+        build_ms = statistics.median(bt)
+        tokens = w.B * w.Hkv * w.N
+        flops = 2.0 * w.B * w.Hkv * (w.N - w.sink - w.window) * w.k_per_seg * w.d * w.iters
+        build = {"ms": build_ms, "tokens_indexed_per_s": tokens / (build_ms * 1e-3),
+                 "assign_tflop": flops * 1e-12,
+                 "assign_tflops_over_whole_build": flops / (build_ms * 1e-3) * 1e-12,
+                 "launches": 2 + 3 * w.iters + 1}
+    assert ix.status() == 0
+
+    dec = wl.Decoder(ix, w.Hq, r)
+
+    def step():
+        dec(q, K, V, with_topk=False)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+
+    # ---- timed region 1: the fused call (value)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    gpu_uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    sampler = ClockSampler("GPU-" + str(gpu_uuid) if gpu_uuid else "")
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- timed region 2: the same step as its four stage calls, for the
+    # per-kernel durations of the roofline
+    names = ["score", "select", "attend", "merge"]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e = kev[i]
+        e[0].record(stream)
+        dec.score(q)
+        e[1].record(stream)
+        dec.select()
+        e[2].record(stream)
+        dec.attend(q, K, V)
+        e[3].record(stream)
+        dec.merge()
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert dec.status() == 0
+    kern_ms = {n: statistics.mean(kev[i][j].elapsed_time(kev[i][j + 1])
+                                  for i in range(args.steps)) for j, n in enumerate(names)}
+
+    # ---- e2e through the public API with host buffers
+    q_host = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_host.copy_(q)
+    out_host = torch.empty(dec.out.shape, dtype=torch.float32, pin_memory=True)
+    lse_host = torch.empty(dec.lse.shape, dtype=torch.float32, pin_memory=True)
+    q_dev = torch.empty_like(q)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q_dev.copy_(q_host, non_blocking=True)
+        out, lse, _ = dec(q_dev, K, V, with_topk=False)
+        out_host.copy_(out, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    assert torch.isfinite(out_host).all()
+
+    # ---- bytes
+    dec(q, K, V, with_topk=True)
+    torch.cuda.synchronize()
+    C = cfg.n_clusters
+    n_size = ix.size
+    kbar_bytes = w.B * w.Hkv * C * (w.d * 4 + 4)
+    vsum_bytes = w.B * w.Hkv * C * (w.d * 4 + 4)
+    steady_bytes = w.B * w.Hkv * (w.sink + w.window) * w.d * 2 * 2
+    retr_bytes = retrieved_unique_bytes(dec.topk[..., :r].contiguous(), n_size, w.Hq // w.Hkv)
+    step_bytes = kbar_bytes + vsum_bytes + steady_bytes + retr_bytes
+    kern_bytes = {"score": kbar_bytes, "select": 0, "attend": vsum_bytes + steady_bytes + retr_bytes,
+                  "merge": 0}
+
+    ms = statistics.mean(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms, statistics.mean(e2e_ms)], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_mean = t.tolist()
+    else:
+        e2e_mean = statistics.mean(e2e_ms)
+    queries = w.B * ws
+    value = queries / (ms * 1e-3)
+
+    # dominant HBM-bound kernel (select and merge move no algorithmic HBM bytes)
+    dom = max(("score", "attend"), key=lambda n: kern_ms[n])
+    hbm_peak = float(pk["hbm_gbs"])
+    ach = kern_bytes[dom] / (kern_ms[dom] * 1e-3) / 1e9 if kern_bytes[dom] else 0.0
+    roofline = {"kernel": dom + "_kernel", "bound": "hbm", "achieved": ach, "peak": hbm_peak,
+                "unit": "GB/s", "frac": ach / hbm_peak,
+                "traffic": recorded_traffic(dom, w.name),
+                "algorithmic_bytes_per_launch": kern_bytes[dom],
+                "peak_source": pk_kind + " (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured"
+                else "fallback 6.4 TB/s"}
+    step_gbs = step_bytes / (ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        index_np = {
+            "size": ix.size[0, 0].cpu().numpy().astype(np.int64),
+            "centroid_key": ix.centroid_key[0, 0].double().cpu().numpy(),
+            "value_sum": ix.value_sum[0, 0].double().cpu().numpy(),
+            "perm": ix.perm[0, 0].cpu().numpy().astype(np.int64),
+            "offset": ix.offset[0, 0].cpu().numpy().astype(np.int64),
+        }
+        val, desc, _ = oracle_decode_sample(w, g_np, index_np, r, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": desc, "host_cpus": os.cpu_count()}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, r),
+        "roofline": roofline,
+        "hbm": {"algorithmic_bytes_per_step": step_bytes, "achieved_gbs": step_gbs,
+                "frac_of_measured": step_gbs / hbm_peak, "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                "bytes": {"centroid_keys": kbar_bytes, "value_sums_sizes": vsum_bytes,
+                          "steady_kv": steady_bytes, "retrieved_kv_unique": retr_bytes}},
+        "kernels_ms": kern_ms,
+        "cpu_baseline": cpu,
+        "e2e": {"value": queries / (e2e_mean * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": dec.out.numel() * 4 + dec.lse.numel() * 4,
+                "ms_per_step": e2e_mean},
+        "gpu_launches": 4 * args.steps * 2,
+        "clocks": clocks,
+        "build": build,
+        "full_pass_ms": (build["ms"] + ms) if build else None,
+        "wall_s_timed_region_1": wall,
+        "setup_seconds": {"generate": t_gen},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,285 @@
+"""PyTorch-facing binding of libwi: allocates device tensors with torch and
+passes their pointers to the C ABI.  Every step of the index build and of the
+decode runs in libwi's CUDA kernels; this module only marshals arguments.
+
+Method: "RetroInfer: A Vector Storage Engine for Scalable Long-Context LLM
+Inference" -- wave index (technical summary §2.A), segmented clustering (§3).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import _lib as L
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s must live on %s" % (name, device))
+
+
+@dataclasses.dataclass
+class IndexConfig:
+    B: int
+    Hkv: int
+    N: int
+    sink: int
+    window: int
+    seg_len: int
+    k_per_seg: int
+    iters: int
+    d: int = 128
+
+    @property
+    def n_seg(self) -> int:
+        return -(-self.N // self.seg_len)
+
+    @property
+    def n_clusters(self) -> int:
+        return self.n_seg * self.k_per_seg
+
+    @property
+    def n_idx(self) -> int:
+        return self.N - self.sink - self.window
+
+    def params(self) -> L.BuildParams:
+        return L.BuildParams(self.B, self.Hkv, self.N, self.d, self.sink, self.window,
+                             self.seg_len, self.k_per_seg, self.iters)
+
+
+_FIELD_DTYPES = {
+    "centroid_key": torch.float32, "unit_centroid": torch.bfloat16, "value_sum": torch.float32,
+    "size": torch.int32, "offset": torch.int32, "perm": torch.int32, "assign": torch.int32,
+    "k_sorted": torch.bfloat16, "v_sorted": torch.bfloat16,
+}
+
+
+def index_sizes(cfg: IndexConfig) -> Dict[str, int]:
+    """Bytes of every index array (wi_index_sizes); no device work."""
+    out = (ctypes.c_size_t * len(L.FIELDS))()
+    L.check(L.lib().wi_index_sizes(ctypes.byref(cfg.params()), out), "wi_index_sizes")
+    return {name: int(out[i]) for i, name in enumerate(L.FIELDS)}
+
+
+def build_workspace_bytes(cfg: IndexConfig) -> int:
+    n = L.lib().wi_build_workspace_bytes(ctypes.byref(cfg.params()))
+    if n == 0:
+        raise L.WIError(L.WI_ERR_INVALID_ARG, "wi_build_workspace_bytes")
+    return int(n)
+
+
+class WaveIndex:
+    """The caller-owned device arrays of a wave index and the wi_index struct
+    that points at them."""
+
+    def __init__(self, cfg: IndexConfig, device):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        B, H, N, C, d, n = cfg.B, cfg.Hkv, cfg.N, cfg.n_clusters, cfg.d, cfg.n_idx
+        shapes = {
+            "centroid_key": (B, H, C, d), "unit_centroid": (B, H, C, d),
+            "value_sum": (B, H, C, d), "size": (B, H, C), "offset": (B, H, C + 1),
+            "perm": (B, H, n), "assign": (B, H, N), "k_sorted": (B, H, n, d),
+            "v_sorted": (B, H, n, d),
+        }
+        sizes = index_sizes(cfg)
+        self.tensors: Dict[str, torch.Tensor] = {}
+        for name in L.FIELDS:
+            t = torch.empty(shapes[name], dtype=_FIELD_DTYPES[name], device=self.device)
+            assert t.numel() * t.element_size() == sizes[name], name
+            self.tensors[name] = t
+        self.struct = L.IndexStruct(*[t.data_ptr() for t in (self.tensors[f] for f in L.FIELDS)])
+        self.workspace = torch.zeros(build_workspace_bytes(cfg), dtype=torch.uint8,
+                                     device=self.device)
+
+    def __getattr__(self, name):
+        tensors = self.__dict__.get("tensors")
+        if tensors is not None and name in tensors:
+            return tensors[name]
+        raise AttributeError(name)
+
+    @property
+    def n_clusters(self) -> int:
+        return self.cfg.n_clusters
+
+    def _kv(self, K, V=None):
+        c = self.cfg
+        _need(K, "K", torch.bfloat16, (c.B, c.Hkv, c.N, c.d), self.device)
+        if V is not None:
+            _need(V, "V", torch.bfloat16, (c.B, c.Hkv, c.N, c.d), self.device)
+
+    # individual build steps ---------------------------------------------
+    def init(self, K, stream=None):
+        self._kv(K)
+        L.check(L.lib().wi_build_init(ctypes.byref(self.cfg.params()), _ptr(K),
+                                      ctypes.byref(self.struct), _ptr(self.workspace),
+                                      self.workspace.numel(), _stream(stream)), "wi_build_init")
+
+    def assign_step(self, K, stream=None):
+        self._kv(K)
+        L.check(L.lib().wi_kmeans_assign(ctypes.byref(self.cfg.params()), _ptr(K),
+                                         ctypes.byref(self.struct), _ptr(self.workspace),
+                                         self.workspace.numel(), _stream(stream)),
+                "wi_kmeans_assign")
+
+    def update_step(self, K, stream=None):
+        self._kv(K)
+        L.check(L.lib().wi_kmeans_update(ctypes.byref(self.cfg.params()), _ptr(K),
+                                         ctypes.byref(self.struct), _ptr(self.workspace),
+                                         self.workspace.numel(), _stream(stream)),
+                "wi_kmeans_update")
+
+    def finalize(self, K, V, stream=None):
+        self._kv(K, V)
+        L.check(L.lib().wi_build_finalize(ctypes.byref(self.cfg.params()), _ptr(K), _ptr(V),
+                                          ctypes.byref(self.struct), _ptr(self.workspace),
+                                          self.workspace.numel(), _stream(stream)),
+                "wi_build_finalize")
+
+    def build(self, K, V, stream=None):
+        self._kv(K, V)
+        L.check(L.lib().wi_build_index(ctypes.byref(self.cfg.params()), _ptr(K), _ptr(V),
+                                       ctypes.byref(self.struct), _ptr(self.workspace),
+                                       self.workspace.numel(), _stream(stream)),
+                "wi_build_index")
+        return self
+
+    def status(self, stream=None) -> int:
+        return sync_status(self.workspace, stream)
+
+
+def build_index(K: torch.Tensor, V: torch.Tensor, sink: int, window: int, seg_len: int,
+                k_per_seg: int, iters: int, stream=None) -> WaveIndex:
+    """Build the wave index of K, V (bf16 [B, Hkv, N, 128], on the GPU)."""
+    B, H, N, d = K.shape
+    cfg = IndexConfig(B, H, N, sink, window, seg_len, k_per_seg, iters, d)
+    return WaveIndex(cfg, K.device).build(K, V, stream)
+
+
+def sync_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and read-and-clear the device status word."""
+    st = ctypes.c_int(0)
+    L.check(L.lib().wi_sync_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
+            "wi_sync_status")
+    return st.value
+
+
+class Decoder:
+    """Decode attention against one WaveIndex with fixed (Hq, r, scale); owns
+    its workspace and output buffers."""
+
+    def __init__(self, index: WaveIndex, Hq: int, r: int, scale: Optional[float] = None):
+        c = index.cfg
+        self.index = index
+        self.Hq = Hq
+        self.r = r
+        self.scale = 1.0 / math.sqrt(c.d) if scale is None else float(scale)
+        self.params = L.DecodeParams(c.B, Hq, c.Hkv, c.N, c.d, c.sink, c.window, r, self.scale)
+        lay = L.DecodeLayout()
+        L.check(L.lib().wi_decode_workspace_layout(ctypes.byref(self.params), c.n_clusters,
+                                                   ctypes.byref(lay)), "wi_decode_workspace_layout")
+        self.layout = lay
+        dev = index.device
+        self.workspace = torch.zeros(lay.total, dtype=torch.uint8, device=dev)
+        self.out = torch.empty((c.B, Hq, c.d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((c.B, Hq), dtype=torch.float32, device=dev)
+        self.topk = torch.empty((c.B, Hq, max(r, 1)), dtype=torch.int32, device=dev)
+
+    def _q(self, q):
+        c = self.index.cfg
+        _need(q, "q", torch.bfloat16, (c.B, self.Hq, c.d), self.index.device)
+
+    def __call__(self, q, K, V, stream=None, with_topk: bool = True):
+        """out [B,Hq,128] f32, lse [B,Hq] f32, topk ids [B,Hq,r] i32."""
+        self._q(q)
+        self.index._kv(K, V)
+        topk = self.topk if (with_topk and self.r > 0) else None
+        L.check(L.lib().wi_decode_attention(
+            ctypes.byref(self.params), _ptr(q), _ptr(K), _ptr(V), ctypes.byref(self.index.struct),
+            _ptr(self.out), _ptr(self.lse), _ptr(topk), _ptr(self.workspace),
+            self.workspace.numel(), _stream(stream)), "wi_decode_attention")
+        return self.out, self.lse, (self.topk[..., :self.r] if topk is not None else None)
+
+    # stages -------------------------------------------------------------
+    def score(self, q, stream=None):
+        self._q(q)
+        L.check(L.lib().wi_decode_score(ctypes.byref(self.params), _ptr(q),
+                                        ctypes.byref(self.index.struct), _ptr(self.workspace),
+                                        self.workspace.numel(), _stream(stream)),
+                "wi_decode_score")
+
+    def select(self, stream=None, with_topk: bool = False):
+        topk = self.topk if (with_topk and self.r > 0) else None
+        L.check(L.lib().wi_decode_select(ctypes.byref(self.params), ctypes.byref(self.index.struct),
+                                         _ptr(topk), _ptr(self.workspace), self.workspace.numel(),
+                                         _stream(stream)), "wi_decode_select")
+
+    def attend(self, q, K, V, stream=None):
+        self._q(q)
+        self.index._kv(K, V)
+        L.check(L.lib().wi_decode_attend(ctypes.byref(self.params), _ptr(q), _ptr(K), _ptr(V),
+                                         ctypes.byref(self.index.struct), _ptr(self.workspace),
+                                         self.workspace.numel(), _stream(stream)),
+                "wi_decode_attend")
+
+    def merge(self, stream=None):
+        L.check(L.lib().wi_decode_merge(ctypes.byref(self.params), ctypes.byref(self.index.struct),
+                                        _ptr(self.out), _ptr(self.lse), _ptr(self.workspace),
+                                        self.workspace.numel(), _stream(stream)),
+                "wi_decode_merge")
+        return self.out, self.lse
+
+    # workspace views ------------------------------------------------------
+    def _view(self, off: int, count: int, dtype, shape):
+        nbytes = count * torch.tensor([], dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype).view(shape)
+
+    def scores(self) -> torch.Tensor:
+        c = self.index.cfg
+        return self._view(self.layout.scores, c.B * self.Hq * c.n_clusters, torch.float32,
+                          (c.B, self.Hq, c.n_clusters))
+
+    def head_max(self) -> torch.Tensor:
+        c = self.index.cfg
+        return self._view(self.layout.head_max, c.B * self.Hq, torch.float32, (c.B, self.Hq))
+
+    def selected(self) -> Tuple[torch.Tensor, torch.Tensor]:
+        c = self.index.cfg
+        rs = max(self.r, 1)
+        ids = self._view(self.layout.selected, c.B * self.Hq * rs, torch.int32, (c.B, self.Hq, rs))
+        pre = self._view(self.layout.sel_prefix, c.B * self.Hq * (self.r + 1), torch.int32,
+                         (c.B, self.Hq, self.r + 1))
+        return ids[..., :self.r], pre
+
+    def status(self, stream=None) -> int:
+        return sync_status(self.workspace, stream)
+
+
+def decode_attention(q, K, V, index: WaveIndex, r: int, scale: Optional[float] = None,
+                     stream=None):
+    """One tripartite decode step: returns (out, lse, topk_ids)."""
+    dec = Decoder(index, q.shape[1], r, scale)
+    return dec(q, K, V, stream)

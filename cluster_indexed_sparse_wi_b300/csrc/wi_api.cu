@@ -1,0 +1,472 @@
+// C ABI of libwi (declared in include/wi.h): argument validation, workspace
+// layout, and kernel enqueueing on the caller's stream.  No device memory is
+// allocated here and nothing synchronises except wi_sync_status.
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "wi.h"
+#include "wi_internal.h"
+
+using wi::BuildArgs;
+using wi::DecodeArgs;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;  // status word + reserved counters
+std::atomic<int> g_inject{0};         // wi_debug_inject request
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+int device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WI_ERR_LAUNCH;
+  static int checked[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  if (dev >= 0 && dev < 64 && checked[dev] != 0) return checked[dev] == 1 ? WI_OK : WI_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return WI_ERR_LAUNCH;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) checked[dev] = ok ? 1 : 2;
+  return ok ? WI_OK : WI_ERR_UNSUPPORTED;
+}
+
+int check_build(const wi_build_params* p) {
+  if (p == nullptr) return WI_ERR_INVALID_ARG;
+  if (p->B < 1 || p->Hkv < 1 || p->N < 1 || p->sink < 0 || p->window < 0 || p->iters < 1 ||
+      p->seg_len < 1 || p->k_per_seg < 1)
+    return WI_ERR_INVALID_ARG;
+  if ((long long)p->sink + p->window > p->N) return WI_ERR_INVALID_ARG;
+  if (p->d != WI_HEAD_DIM) return WI_ERR_UNSUPPORTED;
+  if (p->seg_len > WI_MAX_SEG_LEN || p->k_per_seg > WI_MAX_K_PER_SEG) return WI_ERR_UNSUPPORTED;
+  if (p->N > (1 << 30)) return WI_ERR_UNSUPPORTED;
+  const long long n_seg = ((long long)p->N + p->seg_len - 1) / p->seg_len;
+  if (n_seg * p->k_per_seg > WI_MAX_CLUSTERS) return WI_ERR_UNSUPPORTED;
+  return WI_OK;
+}
+
+int n_clusters_of(const wi_build_params* p) {
+  return (int)(((long long)p->N + p->seg_len - 1) / p->seg_len) * p->k_per_seg;
+}
+
+size_t build_ws_bytes(const wi_build_params* p) {
+  return kStatusBytes + align256((size_t)p->B * p->Hkv * p->N * sizeof(float));
+}
+
+int fill_build_args(const wi_build_params* p, const void* K, const void* V, wi_index* ix,
+                    void* ws, size_t ws_bytes, BuildArgs* a) {
+  int st = check_build(p);
+  if (st != WI_OK) return st;
+  if (ix == nullptr || ws == nullptr || K == nullptr) return WI_ERR_INVALID_ARG;
+  if (ws_bytes < build_ws_bytes(p)) return WI_ERR_WORKSPACE;
+  if (!aligned(ws, 256) || !aligned(K, 16) || (V != nullptr && !aligned(V, 16)))
+    return WI_ERR_ALIGNMENT;
+  memset(a, 0, sizeof(*a));
+  a->B = p->B;
+  a->Hkv = p->Hkv;
+  a->N = p->N;
+  a->sink = p->sink;
+  a->window = p->window;
+  a->L = p->seg_len;
+  a->k = p->k_per_seg;
+  a->n_seg = (int)(((long long)p->N + p->seg_len - 1) / p->seg_len);
+  a->C = a->n_seg * a->k;
+  a->N_idx = p->N - p->sink - p->window;
+  a->K = static_cast<const uint16_t*>(K);
+  a->V = static_cast<const uint16_t*>(V);
+  a->status = static_cast<int*>(ws);
+  a->norms = reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes);
+  a->kbar = ix->centroid_key;
+  a->mu = static_cast<uint16_t*>(ix->unit_centroid);
+  a->vsum = ix->value_sum;
+  a->size = ix->size;
+  a->offset = ix->offset;
+  a->perm = ix->perm;
+  a->assign = ix->assign;
+  a->ksorted = static_cast<uint16_t*>(ix->k_sorted);
+  a->vsorted = static_cast<uint16_t*>(ix->v_sorted);
+  return WI_OK;
+}
+
+// Pointers a build step needs, by step.
+enum Need { kNeedInit = 1, kNeedAssign = 2, kNeedUpdate = 4, kNeedFinal = 8 };
+
+int check_index_ptrs(const BuildArgs& a, int need) {
+  const void* req[9] = {nullptr};
+  int n = 0;
+  req[n++] = a.mu;
+  req[n++] = a.assign;
+  if (need & (kNeedUpdate | kNeedFinal)) {
+    req[n++] = a.size;
+    req[n++] = a.offset;
+    req[n++] = a.perm;
+  }
+  if (need & kNeedFinal) {
+    req[n++] = a.kbar;
+    req[n++] = a.vsum;
+    req[n++] = a.ksorted;
+    req[n++] = a.vsorted;
+  }
+  for (int i = 0; i < n; ++i) {
+    // arrays with N_idx rows (perm, k_sorted, v_sorted) may be NULL when N_idx == 0
+    const bool may_be_null = a.N_idx == 0 && (req[i] == a.perm || req[i] == a.ksorted ||
+                                              req[i] == a.vsorted);
+    if (req[i] == nullptr && !may_be_null) return WI_ERR_INVALID_ARG;
+    if (!aligned(req[i], 16)) return WI_ERR_ALIGNMENT;
+  }
+  if ((need & kNeedFinal) && a.V == nullptr) return WI_ERR_INVALID_ARG;
+  return WI_OK;
+}
+
+int check_recorded(const wi_build_params* p, const wi_index* ix) {
+  const int C = n_clusters_of(p);
+  if (ix->B != p->B || ix->Hkv != p->Hkv || ix->N != p->N || ix->d != p->d ||
+      ix->sink != p->sink || ix->window != p->window || ix->seg_len != p->seg_len ||
+      ix->k_per_seg != p->k_per_seg || ix->n_clusters != C)
+    return WI_ERR_INDEX_MISMATCH;
+  return WI_OK;
+}
+
+void record(const wi_build_params* p, wi_index* ix) {
+  ix->B = p->B;
+  ix->Hkv = p->Hkv;
+  ix->N = p->N;
+  ix->d = p->d;
+  ix->sink = p->sink;
+  ix->window = p->window;
+  ix->seg_len = p->seg_len;
+  ix->k_per_seg = p->k_per_seg;
+  ix->n_clusters = n_clusters_of(p);
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? WI_OK : WI_ERR_LAUNCH; }
+
+// ---------------------------------------------------------------- decode
+int check_decode(const wi_decode_params* p, int C) {
+  if (p == nullptr) return WI_ERR_INVALID_ARG;
+  if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->N < 1 || p->sink < 0 || p->window < 0 ||
+      p->r < 0 || C < 1)
+    return WI_ERR_INVALID_ARG;
+  if ((long long)p->sink + p->window > p->N || p->r > C) return WI_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return WI_ERR_INVALID_ARG;
+  const int G = p->Hq / p->Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return WI_ERR_UNSUPPORTED;
+  if (p->d != WI_HEAD_DIM || C > WI_MAX_CLUSTERS || p->N > (1 << 30)) return WI_ERR_UNSUPPORTED;
+  if (!(p->scale == p->scale)) return WI_ERR_INVALID_ARG;
+  return WI_OK;
+}
+
+int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
+  const int st = check_decode(p, C);
+  if (st != WI_OK) return st;
+  memset(L, 0, sizeof(*L));
+  const long long heads = (long long)p->B * p->Hq;
+  const long long n_idx = (long long)p->N - p->sink - p->window;
+  // expected exact tokens per query head: steady zone + r average clusters
+  const long long est_tokens = p->sink + p->window + ((long long)p->r * n_idx + C - 1) / C;
+  long long splits = (est_tokens + 191) / 192;
+  const long long min_splits = (2 * 148 + heads - 1) / heads;
+  if (splits < min_splits) splits = min_splits;
+  if (splits > 128) splits = 128;
+  if (splits < 1) splits = 1;
+  L->att_splits = (int)splits;
+  L->est_chunk_clusters = 256;
+  L->est_chunks = (C + L->est_chunk_clusters - 1) / L->est_chunk_clusters;
+  const int r_slots = p->r > 0 ? p->r : 1;
+  const int n_words = (C + 31) / 32;
+  size_t off = kStatusBytes;
+  L->scores = off;
+  off += align256((size_t)heads * C * 4);
+  L->head_max = off;
+  off += align256((size_t)heads * 4);
+  L->selected = off;
+  off += align256((size_t)heads * r_slots * 4);
+  L->sel_prefix = off;
+  off += align256((size_t)heads * (p->r + 1) * 4);
+  L->sel_mask = off;
+  off += align256((size_t)heads * n_words * 4);
+  L->att_partials = off;
+  off += align256((size_t)heads * L->att_splits * wi::kPartStride * 4);
+  L->est_partials = off;
+  off += align256((size_t)heads * L->est_chunks * wi::kPartStride * 4);
+  L->total = off;
+  return WI_OK;
+}
+
+int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, const void* V,
+                     const wi_index* ix, void* ws, size_t ws_bytes, DecodeArgs* a,
+                     bool need_kv) {
+  if (ix == nullptr || ws == nullptr) return WI_ERR_INVALID_ARG;
+  wi_decode_layout L;
+  int st = decode_layout(p, ix->n_clusters, &L);
+  if (st != WI_OK) return st;
+  if (ix->B != p->B || ix->Hkv != p->Hkv || ix->N != p->N || ix->d != p->d ||
+      ix->sink != p->sink || ix->window != p->window)
+    return WI_ERR_INDEX_MISMATCH;
+  if (ws_bytes < L.total) return WI_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return WI_ERR_ALIGNMENT;
+  const bool no_idx = p->N - p->sink - p->window == 0;  // sorted arrays may be NULL then
+  const void* req[] = {ix->centroid_key, ix->value_sum, ix->size, ix->offset,
+                       ix->k_sorted, ix->v_sorted};
+  for (int i = 0; i < 6; ++i) {
+    if (req[i] == nullptr && !(no_idx && i >= 4)) return WI_ERR_INVALID_ARG;
+    if (!aligned(req[i], 16)) return WI_ERR_ALIGNMENT;
+  }
+  if (need_kv) {
+    if (q == nullptr || K == nullptr || V == nullptr) return WI_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16)) return WI_ERR_ALIGNMENT;
+  }
+  memset(a, 0, sizeof(*a));
+  char* w = static_cast<char*>(ws);
+  a->B = p->B;
+  a->Hq = p->Hq;
+  a->Hkv = p->Hkv;
+  a->G = p->Hq / p->Hkv;
+  a->N = p->N;
+  a->sink = p->sink;
+  a->window = p->window;
+  a->r = p->r;
+  a->C = ix->n_clusters;
+  a->N_idx = p->N - p->sink - p->window;
+  a->n_words = (a->C + 31) / 32;
+  a->scale = p->scale;
+  a->q = static_cast<const uint16_t*>(q);
+  a->K = static_cast<const uint16_t*>(K);
+  a->V = static_cast<const uint16_t*>(V);
+  a->kbar = ix->centroid_key;
+  a->vsum = ix->value_sum;
+  a->size = ix->size;
+  a->offset = ix->offset;
+  a->ksorted = static_cast<const uint16_t*>(ix->k_sorted);
+  a->vsorted = static_cast<const uint16_t*>(ix->v_sorted);
+  a->status = reinterpret_cast<int*>(w);
+  a->scores = reinterpret_cast<float*>(w + L.scores);
+  a->head_max = reinterpret_cast<float*>(w + L.head_max);
+  a->sel_ids = reinterpret_cast<int*>(w + L.selected);
+  a->sel_prefix = reinterpret_cast<int*>(w + L.sel_prefix);
+  a->sel_mask = reinterpret_cast<uint32_t*>(w + L.sel_mask);
+  a->att_part = reinterpret_cast<float*>(w + L.att_partials);
+  a->est_part = reinterpret_cast<float*>(w + L.est_partials);
+  a->att_splits = L.att_splits;
+  a->est_chunks = L.est_chunks;
+  a->est_chunk_clusters = L.est_chunk_clusters;
+  return WI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wi_index_sizes(const wi_build_params* p, size_t* bytes_out) {
+  const int st = check_build(p);
+  if (st != WI_OK) return st;
+  if (bytes_out == nullptr) return WI_ERR_INVALID_ARG;
+  const size_t heads = (size_t)p->B * p->Hkv;
+  const size_t C = (size_t)n_clusters_of(p);
+  const size_t n_idx = (size_t)(p->N - p->sink - p->window);
+  bytes_out[WI_FIELD_CENTROID_KEY] = heads * C * WI_HEAD_DIM * 4;
+  bytes_out[WI_FIELD_UNIT_CENTROID] = heads * C * WI_HEAD_DIM * 2;
+  bytes_out[WI_FIELD_VALUE_SUM] = heads * C * WI_HEAD_DIM * 4;
+  bytes_out[WI_FIELD_SIZE] = heads * C * 4;
+  bytes_out[WI_FIELD_OFFSET] = heads * (C + 1) * 4;
+  bytes_out[WI_FIELD_PERM] = heads * n_idx * 4;
+  bytes_out[WI_FIELD_ASSIGN] = heads * (size_t)p->N * 4;
+  bytes_out[WI_FIELD_K_SORTED] = heads * n_idx * WI_HEAD_DIM * 2;
+  bytes_out[WI_FIELD_V_SORTED] = heads * n_idx * WI_HEAD_DIM * 2;
+  return WI_OK;
+}
+
+size_t wi_build_workspace_bytes(const wi_build_params* p) {
+  return check_build(p) == WI_OK ? build_ws_bytes(p) : 0;
+}
+
+int wi_build_init(const wi_build_params* p, const void* K, wi_index* index, void* workspace,
+                  size_t workspace_bytes, wi_stream_t stream) {
+  BuildArgs a;
+  int st = fill_build_args(p, K, nullptr, index, workspace, workspace_bytes, &a);
+  if (st != WI_OK) return st;
+  if ((st = check_index_ptrs(a, kNeedInit)) != WI_OK) return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  record(p, index);
+  return cuda_status(wi::launch_build_init(a, (cudaStream_t)stream));
+}
+
+int wi_kmeans_assign(const wi_build_params* p, const void* K, wi_index* index, void* workspace,
+                     size_t workspace_bytes, wi_stream_t stream) {
+  BuildArgs a;
+  int st = fill_build_args(p, K, nullptr, index, workspace, workspace_bytes, &a);
+  if (st != WI_OK) return st;
+  if ((st = check_index_ptrs(a, kNeedAssign)) != WI_OK) return st;
+  if ((st = check_recorded(p, index)) != WI_OK) return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  return cuda_status(wi::launch_kmeans_assign(a, (cudaStream_t)stream));
+}
+
+int wi_kmeans_update(const wi_build_params* p, const void* K, wi_index* index, void* workspace,
+                     size_t workspace_bytes, wi_stream_t stream) {
+  BuildArgs a;
+  int st = fill_build_args(p, K, nullptr, index, workspace, workspace_bytes, &a);
+  if (st != WI_OK) return st;
+  if ((st = check_index_ptrs(a, kNeedUpdate)) != WI_OK) return st;
+  if ((st = check_recorded(p, index)) != WI_OK) return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = wi::launch_cluster_sort(a, s);
+  if (e == cudaSuccess) e = wi::launch_centroid_update(a, s);
+  return cuda_status(e);
+}
+
+int wi_build_finalize(const wi_build_params* p, const void* K, const void* V, wi_index* index,
+                      void* workspace, size_t workspace_bytes, wi_stream_t stream) {
+  BuildArgs a;
+  int st = fill_build_args(p, K, V, index, workspace, workspace_bytes, &a);
+  if (st != WI_OK) return st;
+  if ((st = check_index_ptrs(a, kNeedFinal)) != WI_OK) return st;
+  if ((st = check_recorded(p, index)) != WI_OK) return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = wi::launch_cluster_sort(a, s);
+  if (e == cudaSuccess) e = wi::launch_finalize_stats(a, s);
+  return cuda_status(e);
+}
+
+int wi_build_index(const wi_build_params* p, const void* K, const void* V, wi_index* index,
+                   void* workspace, size_t workspace_bytes, wi_stream_t stream) {
+  BuildArgs a;
+  int st = fill_build_args(p, K, V, index, workspace, workspace_bytes, &a);
+  if (st != WI_OK) return st;
+  if ((st = check_index_ptrs(a, kNeedInit | kNeedAssign | kNeedUpdate | kNeedFinal)) != WI_OK)
+    return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  record(p, index);
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = wi::launch_build_init(a, s);
+  for (int it = 0; it < p->iters && e == cudaSuccess; ++it) {
+    e = wi::launch_kmeans_assign(a, s);
+    if (e == cudaSuccess) e = wi::launch_cluster_sort(a, s);
+    if (e == cudaSuccess) e = wi::launch_centroid_update(a, s);
+  }
+  // the last update sorted the final assignment: size/offset/perm are current
+  if (e == cudaSuccess) e = wi::launch_finalize_stats(a, s);
+  return cuda_status(e);
+}
+
+size_t wi_decode_workspace_bytes(const wi_decode_params* p, int n_clusters) {
+  wi_decode_layout L;
+  return decode_layout(p, n_clusters, &L) == WI_OK ? L.total : 0;
+}
+
+int wi_decode_workspace_layout(const wi_decode_params* p, int n_clusters,
+                               wi_decode_layout* layout_out) {
+  if (layout_out == nullptr) return WI_ERR_INVALID_ARG;
+  return decode_layout(p, n_clusters, layout_out);
+}
+
+int wi_decode_score(const wi_decode_params* p, const void* q, const wi_index* index,
+                    void* workspace, size_t workspace_bytes, wi_stream_t stream) {
+  DecodeArgs a;
+  int st = fill_decode_args(p, q, nullptr, nullptr, index, workspace, workspace_bytes, &a, false);
+  if (st != WI_OK) return st;
+  if (q == nullptr) return WI_ERR_INVALID_ARG;
+  if (!aligned(q, 16)) return WI_ERR_ALIGNMENT;
+  if ((st = device_ok()) != WI_OK) return st;
+  return cuda_status(wi::launch_decode_score(a, (cudaStream_t)stream));
+}
+
+int wi_decode_select(const wi_decode_params* p, const wi_index* index, int32_t* topk_ids,
+                     void* workspace, size_t workspace_bytes, wi_stream_t stream) {
+  DecodeArgs a;
+  int st = fill_decode_args(p, nullptr, nullptr, nullptr, index, workspace, workspace_bytes, &a,
+                            false);
+  if (st != WI_OK) return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  a.topk_out = topk_ids;
+  return cuda_status(wi::launch_decode_select(a, (cudaStream_t)stream));
+}
+
+int wi_decode_attend(const wi_decode_params* p, const void* q, const void* K, const void* V,
+                     const wi_index* index, void* workspace, size_t workspace_bytes,
+                     wi_stream_t stream) {
+  DecodeArgs a;
+  int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, true);
+  if (st != WI_OK) return st;
+  if ((st = device_ok()) != WI_OK) return st;
+  a.inject = g_inject.exchange(0);
+  return cuda_status(wi::launch_decode_attend(a, (cudaStream_t)stream));
+}
+
+int wi_decode_merge(const wi_decode_params* p, const wi_index* index, float* out, float* lse,
+                    void* workspace, size_t workspace_bytes, wi_stream_t stream) {
+  DecodeArgs a;
+  int st = fill_decode_args(p, nullptr, nullptr, nullptr, index, workspace, workspace_bytes, &a,
+                            false);
+  if (st != WI_OK) return st;
+  if (out == nullptr) return WI_ERR_INVALID_ARG;
+  if ((st = device_ok()) != WI_OK) return st;
+  a.out = out;
+  a.lse = lse;
+  return cuda_status(wi::launch_decode_merge(a, (cudaStream_t)stream));
+}
+
+int wi_decode_attention(const wi_decode_params* p, const void* q, const void* K, const void* V,
+                        const wi_index* index, float* out, float* lse, int32_t* topk_ids,
+                        void* workspace, size_t workspace_bytes, wi_stream_t stream) {
+  DecodeArgs a;
+  int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, true);
+  if (st != WI_OK) return st;
+  if (out == nullptr) return WI_ERR_INVALID_ARG;
+  if ((st = device_ok()) != WI_OK) return st;
+  a.out = out;
+  a.lse = lse;
+  a.topk_out = topk_ids;
+  a.inject = g_inject.exchange(0);
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = wi::launch_decode_score(a, s);
+  if (e == cudaSuccess) e = wi::launch_decode_select(a, s);
+  if (e == cudaSuccess) e = wi::launch_decode_attend(a, s);
+  if (e == cudaSuccess) e = wi::launch_decode_merge(a, s);
+  return cuda_status(e);
+}
+
+int wi_sync_status(void* workspace, wi_stream_t stream, int* device_status) {
+  if (workspace == nullptr || device_status == nullptr) return WI_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  int host = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    *device_status = WI_ERR_CUDA;
+    return WI_ERR_CUDA;
+  }
+  *device_status = host;
+  return WI_OK;
+}
+
+const char* wi_status_string(int status) {
+  switch (status) {
+    case WI_OK: return "ok";
+    case WI_ERR_INVALID_ARG: return "invalid argument";
+    case WI_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case WI_ERR_LAUNCH: return "kernel launch failed";
+    case WI_ERR_INDEX_MISMATCH: return "parameters do not match the index";
+    case WI_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case WI_ERR_WORKSPACE: return "workspace too small";
+    case WI_ERR_ALIGNMENT: return "pointer not aligned";
+    case WI_ERR_CUDA: return "CUDA error on the stream";
+    default: return "unknown status";
+  }
+}
+
+int wi_debug_inject(int flags) {
+  g_inject.store(flags & 1);
+  return WI_OK;
+}
+
+const char* wi_version(void) { return "0.1.0"; }
+
+}  // extern "C"

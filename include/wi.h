@@ -1,0 +1,267 @@
+/*
+ * wi.h -- C ABI of libwi: wave-index tripartite decode attention and its
+ * segmented spherical-k-means index build, for one NVIDIA B300 (sm_103a).
+ *
+ * Method: "RetroInfer: A Vector Storage Engine for Scalable Long-Context LLM
+ * Inference".  Technical summary (es) §2.A "Wave Index": a tripartite attention
+ * approximation -- §2.A.1 steady zone (sink tokens and the local window,
+ * attended exactly), §2.A.2 retrieval zone (a spherical-k-means clustering
+ * index; the clusters most similar to the query are attended exactly),
+ * §2.A.3 estimation zone (cluster centroids estimate the remaining tokens);
+ * §3 segmented clustering (k-means on short segments of the sequence, to cut
+ * index-build time at prefill).  Technical summary (ar) §2.a: the estimation
+ * zone uses the cluster centroids and the sum of the value vectors; §2.b the
+ * execution buffer lays retrieved KV out contiguously for FlashAttention-class
+ * kernels.  The pages print no formulas; the exact arithmetic of every call is
+ * stated beside it below.
+ *
+ * Conventions (all calls):
+ *  - Every pointer argument is a DEVICE pointer, allocated and owned by the
+ *    caller, unless its comment says "host".  The library never allocates or
+ *    frees memory and never synchronises, except wi_sync_status.
+ *  - Every call is asynchronous on the given stream (NULL = legacy default
+ *    stream) and returns a wi_status.  Argument errors are found on the host
+ *    before anything is enqueued.  Errors found on the device (an exhausted
+ *    bounded wait) are recorded in the status word at the start of the
+ *    caller's workspace; wi_sync_status reads and clears it.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns (uint16).  K and V use the
+ *    head-major layout [B, Hkv, N, d], contiguous, d = 128; query head h reads
+ *    KV head h / (Hq / Hkv) (grouped-query attention).
+ *  - Pointers must be 16-byte aligned (256-byte aligned for workspaces).
+ *  - Calls that share a workspace must not overlap on the GPU: they race.
+ *  - Workspaces must be zero-filled once before their first use; the library
+ *    leaves their status word and counters at zero after every call that does
+ *    not fail.
+ */
+#ifndef WI_H_
+#define WI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols keep default visibility; everything else is hidden. */
+#if defined(__GNUC__)
+#define WI_API __attribute__((visibility("default")))
+#else
+#define WI_API
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st *wi_stream_t;
+
+typedef enum {
+  WI_OK = 0,
+  WI_ERR_INVALID_ARG = 1,     /* NULL pointer, bad size, bad combination      */
+  WI_ERR_UNSUPPORTED = 2,     /* d != 128, group size not in {1,2,4,8}, limit */
+  WI_ERR_LAUNCH = 3,          /* a CUDA launch or query failed                */
+  WI_ERR_INDEX_MISMATCH = 4,  /* decode params disagree with the index        */
+  WI_ERR_DEVICE_TIMEOUT = 5,  /* a device-side bounded wait ran out           */
+  WI_ERR_WORKSPACE = 6,       /* workspace too small                          */
+  WI_ERR_ALIGNMENT = 7,       /* a pointer is not suitably aligned            */
+  WI_ERR_CUDA = 8             /* wi_sync_status: the stream reported an error */
+} wi_status;
+
+/* Limits of this build. */
+#define WI_HEAD_DIM 128
+#define WI_MAX_K_PER_SEG 512
+#define WI_MAX_SEG_LEN 16384
+#define WI_MAX_CLUSTERS (1 << 20)
+
+/* Index-build parameters.
+ *  B, Hkv, N, d   : sequences, KV heads, context length, head dim (128).
+ *  sink, window   : steady zone = positions [0, sink) and [N - window, N);
+ *                   sink + window <= N.  The index covers the other N_idx =
+ *                   N - sink - window positions.
+ *  seg_len        : segment length; segment s covers absolute positions
+ *                   [s * seg_len, (s + 1) * seg_len) minus the steady zone;
+ *                   n_seg = ceil(N / seg_len), 1 <= seg_len <= WI_MAX_SEG_LEN.
+ *  k_per_seg      : clusters per segment (1..WI_MAX_K_PER_SEG);
+ *                   cluster j of segment s has id c = s * k_per_seg + j and
+ *                   C = n_seg * k_per_seg <= WI_MAX_CLUSTERS.
+ *  iters          : (assign, update) rounds of spherical k-means, >= 1. */
+typedef struct {
+  int B, Hkv, N, d, sink, window, seg_len, k_per_seg, iters;
+} wi_build_params;
+
+/* Decode parameters.
+ *  r     : retrieval budget, clusters per query head, 0 <= r <= C.
+ *  scale : logit scale, normally 1/sqrt(d).
+ *  sink, window must equal the index's. */
+typedef struct {
+  int B, Hq, Hkv, N, d, sink, window, r;
+  float scale;
+} wi_decode_params;
+
+/* The wave index of every (sequence b, KV head g).  The caller allocates
+ * every array (sizes from wi_index_sizes) and fills the pointers; the build
+ * writes the arrays and the scalar fields after the pointers.
+ *   centroid_key  f32  [B,Hkv,C,d]   mean raw key of each cluster (0 if empty)
+ *   unit_centroid bf16 [B,Hkv,C,d]   spherical k-means centroid (unit length)
+ *   value_sum     f32  [B,Hkv,C,d]   sum of the cluster's value vectors
+ *   size          i32  [B,Hkv,C]     members per cluster, n_c
+ *   offset        i32  [B,Hkv,C+1]   start of cluster c in the sorted arrays
+ *   perm          i32  [B,Hkv,N_idx] sorted slot -> absolute position, sorted
+ *                                    by (cluster, position)
+ *   assign        i32  [B,Hkv,N]     position -> cluster id, -1 = steady zone
+ *   k_sorted      bf16 [B,Hkv,N_idx,d]  K rows in perm order
+ *   v_sorted      bf16 [B,Hkv,N_idx,d]  V rows in perm order */
+typedef struct {
+  float *centroid_key;
+  void *unit_centroid;
+  float *value_sum;
+  int32_t *size;
+  int32_t *offset;
+  int32_t *perm;
+  int32_t *assign;
+  void *k_sorted;
+  void *v_sorted;
+  /* recorded by wi_build_index / wi_build_init */
+  int B, Hkv, N, d, sink, window, seg_len, k_per_seg, n_clusters;
+} wi_index;
+
+enum {
+  WI_FIELD_CENTROID_KEY = 0,
+  WI_FIELD_UNIT_CENTROID,
+  WI_FIELD_VALUE_SUM,
+  WI_FIELD_SIZE,
+  WI_FIELD_OFFSET,
+  WI_FIELD_PERM,
+  WI_FIELD_ASSIGN,
+  WI_FIELD_K_SORTED,
+  WI_FIELD_V_SORTED,
+  WI_NUM_FIELDS
+};
+
+/* Bytes of every index array, in WI_FIELD_* order, into host array
+ * bytes_out[WI_NUM_FIELDS].  No device work. */
+WI_API int wi_index_sizes(const wi_build_params *p, size_t *bytes_out);
+
+/* Workspace bytes needed by the build calls (status word + per-token key
+ * norms).  0 on invalid parameters.  No device work. */
+WI_API size_t wi_build_workspace_bytes(const wi_build_params *p);
+
+/* Full index build (technical summary (es) §2.A.2 and §3; (ar) §2.a, §2.b):
+ * wi_build_init, then iters x (wi_kmeans_assign, wi_kmeans_update), then
+ * wi_build_finalize on the last assignment.  K, V: bf16 [B,Hkv,N,d]. */
+WI_API int wi_build_index(const wi_build_params *p, const void *K, const void *V, wi_index *index,
+                   void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
+/* Build step 1: key norms ||k_i|| (f32, into the workspace), assign = -1 on
+ * the steady zone, and the initial centroids: with the m_s indexable keys of
+ * segment s in position order, centroid j = bf16(k_p / ||k_p||) for
+ * p = floor(j * m_s / k_per_seg) (zero when m_s = 0).  Records the index's
+ * scalar fields. */
+WI_API int wi_build_init(const wi_build_params *p, const void *K, wi_index *index, void *workspace,
+                  size_t workspace_bytes, wi_stream_t stream);
+
+/* Build step 2 (one spherical k-means assignment): for every indexable
+ * position i of segment s, assign[i] = s * k_per_seg + argmax_j k_i . mu_j
+ * over the segment's centroids, the lowest j among equal maxima.  The dot
+ * products run on the tensor cores (bf16 operands, f32 accumulation). */
+WI_API int wi_kmeans_assign(const wi_build_params *p, const void *K, wi_index *index, void *workspace,
+                     size_t workspace_bytes, wi_stream_t stream);
+
+/* Build step 3 (one spherical k-means update): a stable counting sort of the
+ * current assignment writes size, offset and perm; then every non-empty
+ * cluster gets mu_j = bf16(normalize(sum over members of k_i / ||k_i||)),
+ * summed in f32 in position order without atomics.  Empty clusters, and
+ * clusters whose member directions sum to zero, keep their centroid. */
+WI_API int wi_kmeans_update(const wi_build_params *p, const void *K, wi_index *index, void *workspace,
+                     size_t workspace_bytes, wi_stream_t stream);
+
+/* Build step 4: from the current assignment, size / offset / perm (stable
+ * counting sort), centroid_key = (sum of member keys) / n_c and value_sum =
+ * sum of member values (f32 sums in position order), and the cluster-sorted
+ * copies k_sorted / v_sorted. */
+WI_API int wi_build_finalize(const wi_build_params *p, const void *K, const void *V, wi_index *index,
+                      void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
+/* Workspace bytes of wi_decode_attention and its stage calls; 0 on invalid
+ * parameters.  n_clusters is the index's C.  No device work. */
+WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_clusters);
+
+/* Byte offsets of the decode workspace regions (host struct), for
+ * inspection of intermediate results.  No device work. */
+typedef struct {
+  size_t scores;        /* f32 [B,Hq,C]    s_c = scale q.kbar_c, -inf if empty   */
+  size_t head_max;      /* f32 [B,Hq]      max_c s_c                            */
+  size_t selected;      /* i32 [B,Hq,r]    retrieved ids ascending, -1 padding   */
+  size_t sel_prefix;    /* i32 [B,Hq,r+1]  exclusive prefix of selected sizes    */
+  size_t sel_mask;      /* u32 [B,Hq,ceil(C/32)] bit c set = c retrieved          */
+  size_t att_partials;  /* f32 [B,Hq,att_splits,2+d]  (m, l, o) in log2 units     */
+  size_t est_partials;  /* f32 [B,Hq,est_chunks,2+d]                             */
+  size_t total;
+  int att_splits, est_chunks, est_chunk_clusters, reserved;
+} wi_decode_layout;
+WI_API int wi_decode_workspace_layout(const wi_decode_params *p, int n_clusters,
+                               wi_decode_layout *layout_out);
+
+/* Tripartite decode attention for one query per (sequence, query head)
+ * (technical summary (es) §2.A; (ar) §2.a):
+ *   s_c  = scale q.centroid_key_c for n_c > 0, -inf otherwise;
+ *   T    = the r largest s_c over non-empty clusters, ties to the lower id;
+ *   S    = steady positions + members of T, logits l_i = scale q.k_i
+ *          (members read from k_sorted / v_sorted, the steady zone from K / V);
+ *   E    = non-empty clusters outside T;
+ *   M    = max(max_S l_i, max_E s_c),
+ *   L    = sum_S e^{l_i - M} + sum_E n_c e^{s_c - M},
+ *   out  = (sum_S e^{l_i - M} v_i + sum_E e^{s_c - M} value_sum_c) / L,
+ *   lse  = M + ln L  (log-sum-exp merge of the three zones).
+ * q: bf16 [B,Hq,d]; out: f32 [B,Hq,d]; lse: f32 [B,Hq] or NULL;
+ * topk_ids: i32 [B,Hq,r] (ascending ids, -1 padding) or NULL.
+ * Equivalent to wi_decode_score, wi_decode_select, wi_decode_attend,
+ * wi_decode_merge in that order. */
+WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const void *K, const void *V,
+                        const wi_index *index, float *out, float *lse, int32_t *topk_ids,
+                        void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
+/* Decode stage 1: cluster scores s into the workspace (centroid scan). */
+WI_API int wi_decode_score(const wi_decode_params *p, const void *q, const wi_index *index,
+                    void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
+/* Decode stage 2: per query head, the retrieval set T (radix select over the
+ * scores; ties to the lower id), its size prefix and bit mask, and the head's
+ * maximum score.  topk_ids may be NULL. */
+WI_API int wi_decode_select(const wi_decode_params *p, const wi_index *index, int32_t *topk_ids,
+                     void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
+/* Decode stage 3: exact attention partials over the steady zone and the
+ * retrieved clusters (split over the token list), and estimation partials
+ * over the other non-empty clusters (split over cluster chunks). */
+WI_API int wi_decode_attend(const wi_decode_params *p, const void *q, const void *K, const void *V,
+                     const wi_index *index, void *workspace, size_t workspace_bytes,
+                     wi_stream_t stream);
+
+/* Decode stage 4: log-sum-exp merge of all partials into out and lse. */
+WI_API int wi_decode_merge(const wi_decode_params *p, const wi_index *index, float *out, float *lse,
+                    void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device status word at the
+ * start of `workspace` into *device_status (host).  Returns WI_OK, or
+ * WI_ERR_CUDA if the stream reported an error (then *device_status is
+ * WI_ERR_CUDA as well). */
+WI_API int wi_sync_status(void *workspace, wi_stream_t stream, int *device_status);
+
+/* Static description of a status code. */
+WI_API const char *wi_status_string(int status);
+
+/* Test hook for the device-side error path (no GPU fault involved): when bit 0
+ * of `flags` is set, the next wi_decode_attention or wi_decode_attend call
+ * makes its first exact-attention block skip its first staging copy.  That
+ * block's bounded wait then runs out after about one second, the block
+ * returns without output, and wi_sync_status reports WI_ERR_DEVICE_TIMEOUT.
+ * The request is consumed by that one call.  Returns WI_OK. */
+WI_API int wi_debug_inject(int flags);
+
+/* Library version, "major.minor.patch". */
+WI_API const char *wi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WI_H_ */

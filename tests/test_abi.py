@@ -1,0 +1,161 @@
+"""The C-ABI library loads, exports every symbol include/wi.h declares, and
+rejects invalid arguments on the host.  CPU only: no call here reaches the
+device (every call below fails validation before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from cluster_indexed_sparse_wi_b300 import build_lib
+    build_lib.build()
+    from cluster_indexed_sparse_wi_b300 import _lib
+    return _lib
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "wi.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*WI_API\s+(?:const\s+)?\w+(?:\s+\w+)?\s*\*?\s*(wi_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_binding_symbols(L):
+    syms = header_symbols()
+    assert syms == L.SYMBOLS
+
+
+def test_library_exports_every_header_symbol(L):
+    lib = L.lib()
+    for s in header_symbols():
+        assert hasattr(lib, s), s
+    out = os.popen("nm -D --defined-only %s" % L.LIB_PATH).read()
+    exported = set(re.findall(r" T (wi_\w+)", out))
+    assert exported == set(header_symbols())
+
+
+def test_status_strings_and_version(L):
+    lib = L.lib()
+    assert lib.wi_status_string(0) == b"ok"
+    assert lib.wi_status_string(L.WI_ERR_DEVICE_TIMEOUT) == b"device-side wait timed out"
+    assert lib.wi_version() == b"0.1.0"
+
+
+def bp(L, **kw):
+    p = dict(B=1, Hkv=2, N=4096, d=128, sink=4, window=64, seg_len=1024, k_per_seg=64, iters=3)
+    p.update(kw)
+    return L.BuildParams(*[p[k] for k in ("B", "Hkv", "N", "d", "sink", "window", "seg_len",
+                                          "k_per_seg", "iters")])
+
+
+def test_index_sizes(L):
+    lib = L.lib()
+    out = (ctypes.c_size_t * 9)()
+    assert lib.wi_index_sizes(ctypes.byref(bp(L)), out) == 0
+    C, n_idx = 4 * 64, 4096 - 68
+    assert out[0] == 2 * C * 128 * 4 and out[1] == 2 * C * 128 * 2
+    assert out[3] == 2 * C * 4 and out[4] == 2 * (C + 1) * 4
+    assert out[5] == 2 * n_idx * 4 and out[6] == 2 * 4096 * 4
+    assert out[7] == 2 * n_idx * 256
+    assert lib.wi_build_workspace_bytes(ctypes.byref(bp(L))) >= 2 * 4096 * 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), 2), (dict(sink=4000, window=100), 1), (dict(iters=0), 1),
+    (dict(seg_len=0), 1), (dict(seg_len=1 << 15), 2), (dict(k_per_seg=513), 2),
+    (dict(N=0), 1), (dict(window=-1), 1),
+])
+def test_build_param_validation(L, kw, code):
+    lib = L.lib()
+    out = (ctypes.c_size_t * 9)()
+    assert lib.wi_index_sizes(ctypes.byref(bp(L, **kw)), out) == code
+    assert lib.wi_build_workspace_bytes(ctypes.byref(bp(L, **kw))) == 0
+    ix = L.IndexStruct()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.wi_build_index(ctypes.byref(bp(L, **kw)), fake, fake, ctypes.byref(ix), fake,
+                              1 << 30, None) == code
+
+
+def test_build_pointer_and_workspace_checks(L):
+    lib = L.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    ix = L.IndexStruct()
+    p = bp(L)
+    # NULL K
+    assert lib.wi_build_index(ctypes.byref(p), None, fake, ctypes.byref(ix), fake, 1 << 30,
+                              None) == L.WI_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.wi_build_index(ctypes.byref(p), fake, fake, ctypes.byref(ix), fake, 16,
+                              None) == L.WI_ERR_WORKSPACE
+    # misaligned K
+    assert lib.wi_build_index(ctypes.byref(p), ctypes.c_void_p((1 << 20) + 8), fake,
+                              ctypes.byref(ix), fake, 1 << 30, None) == L.WI_ERR_ALIGNMENT
+    # index arrays not set (NULL)
+    assert lib.wi_build_index(ctypes.byref(p), fake, fake, ctypes.byref(ix), fake, 1 << 30,
+                              None) == L.WI_ERR_INVALID_ARG
+    # an assign step on an index recorded for other parameters
+    for name in L.FIELDS:
+        setattr(ix, name, 1 << 20)
+    ix.B, ix.Hkv, ix.N, ix.d = 1, 2, 4096, 128
+    ix.sink, ix.window, ix.seg_len, ix.k_per_seg, ix.n_clusters = 4, 64, 1024, 64, 999
+    assert lib.wi_kmeans_assign(ctypes.byref(p), fake, ctypes.byref(ix), fake, 1 << 30,
+                                None) == L.WI_ERR_INDEX_MISMATCH
+
+
+def dp(L, **kw):
+    p = dict(B=1, Hq=8, Hkv=2, N=4096, d=128, sink=4, window=64, r=8, scale=0.088)
+    p.update(kw)
+    return L.DecodeParams(*[p[k] for k in ("B", "Hq", "Hkv", "N", "d", "sink", "window", "r")],
+                          p["scale"])
+
+
+def test_decode_layout(L):
+    lib = L.lib()
+    lay = L.DecodeLayout()
+    assert lib.wi_decode_workspace_layout(ctypes.byref(dp(L)), 256, ctypes.byref(lay)) == 0
+    assert lay.total == lib.wi_decode_workspace_bytes(ctypes.byref(dp(L)), 256)
+    regions = [lay.scores, lay.head_max, lay.selected, lay.sel_prefix, lay.sel_mask,
+               lay.att_partials, lay.est_partials, lay.total]
+    assert regions == sorted(regions) and all(r % 256 == 0 for r in regions)
+    assert lay.head_max - lay.scores >= 8 * 256 * 4
+    assert lay.att_splits >= 1 and lay.est_chunks == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=7), 1), (dict(Hq=6), 2), (dict(Hq=32, Hkv=2), 2), (dict(r=257), 1), (dict(r=-1), 1),
+    (dict(d=96), 2), (dict(sink=5000), 1),
+])
+def test_decode_param_validation(L, kw, code):
+    lib = L.lib()
+    assert lib.wi_decode_workspace_bytes(ctypes.byref(dp(L, **kw)), 256) == 0
+    ix = L.IndexStruct()
+    for name in L.FIELDS:
+        setattr(ix, name, 1 << 20)
+    ix.B, ix.Hkv, ix.N, ix.d, ix.sink, ix.window, ix.n_clusters = 1, 2, 4096, 128, 4, 64, 256
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.wi_decode_attention(ctypes.byref(dp(L, **kw)), fake, fake, fake, ctypes.byref(ix),
+                                   fake, None, None, fake, 1 << 30, None) == code
+
+
+def test_decode_index_mismatch_and_workspace(L):
+    lib = L.lib()
+    ix = L.IndexStruct()
+    for name in L.FIELDS:
+        setattr(ix, name, 1 << 20)
+    ix.B, ix.Hkv, ix.N, ix.d, ix.sink, ix.window, ix.n_clusters = 1, 2, 4096, 128, 4, 32, 256
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.wi_decode_attention(ctypes.byref(dp(L)), fake, fake, fake, ctypes.byref(ix), fake,
+                                   None, None, fake, 1 << 30, None) == L.WI_ERR_INDEX_MISMATCH
+    ix.window = 64
+    assert lib.wi_decode_attention(ctypes.byref(dp(L)), fake, fake, fake, ctypes.byref(ix), fake,
+                                   None, None, fake, 64, None) == L.WI_ERR_WORKSPACE
+    assert lib.wi_decode_attention(ctypes.byref(dp(L)), fake, fake, fake, ctypes.byref(ix), None,
+                                   None, None, fake, 1 << 30, None) == L.WI_ERR_INVALID_ARG
+    assert lib.wi_decode_attention(ctypes.byref(dp(L)), fake, fake, fake, ctypes.byref(ix), fake,
+                                   None, None, ctypes.c_void_p((1 << 20) + 16), 1 << 30,
+                                   None) == L.WI_ERR_ALIGNMENT

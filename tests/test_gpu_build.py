@@ -1,0 +1,173 @@
+"""GPU parity of the index build against the CPU oracle, one step at a time:
+each step takes the GPU's own previous state as the oracle's input, so a
+rounding difference in one iteration does not cascade into the next.
+
+Rules: key norms rel 1e-6; centroids within 1 bf16 ulp per component;
+assignments bit-exact except where the oracle's cosines of the two choices
+differ by less than 1e-5 (a tie); size / offset / perm bit-exact; mean keys and
+value sums within 1e-5 of the row's scale; sorted K/V copies bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import wave_index as wi
+from workloads import WORKLOADS, generate
+from tests._util import bf16_tensor, f64
+
+pytestmark = pytest.mark.gpu
+
+COS_TIE = 1e-5
+
+CASES = {
+    "tiny_4k_1h": dict(B=1, Hkv=1, N=4096, sink=4, window=64, seg_len=4096, k=64, iters=10),
+    "multi_seg_ragged": dict(B=2, Hkv=2, N=20000, sink=4, window=300, seg_len=4096, k=128,
+                             iters=3),
+    "k100_short_tail": dict(B=1, Hkv=1, N=9000, sink=4, window=16, seg_len=2048, k=100, iters=2),
+    "segment_below_k": dict(B=1, Hkv=1, N=1200, sink=4, window=16, seg_len=512, k=300, iters=2),
+}
+
+
+def make(case, seed=5):
+    c = CASES[case]
+    w = WORKLOADS["llama3_8b_128k_b1"].replace(
+        B=c["B"], Hq=c["Hkv"], Hkv=c["Hkv"], N=c["N"], sink=c["sink"], window=c["window"],
+        seg_len=c["seg_len"], k_per_seg=c["k"], iters=c["iters"],
+        planted_per_seg=max(4, c["k"] // 2), seeds=tuple(seed + 7 * b for b in range(c["B"])))
+    g = generate(w, want_q=False)
+    import cluster_indexed_sparse_wi_b300 as wl
+    cfg = wl.IndexConfig(c["B"], c["Hkv"], c["N"], c["sink"], c["window"], c["seg_len"], c["k"],
+                         c["iters"])
+    return c, g, cfg
+
+
+def ulp_ok(a, b):
+    m = np.maximum(np.abs(a), np.abs(b))
+    ulp = np.where(m > 0, 2.0 ** (np.floor(np.log2(np.where(m > 0, m, 1.0))) - 7), 0.0)
+    return np.abs(a - b) <= ulp + 1e-30
+
+
+def seg_positions(cfg):
+    return wi.segment_positions(cfg.N, cfg.sink, cfg.window, cfg.seg_len)
+
+
+def dl(t):
+    return t.detach().cpu().double().numpy() if t.is_floating_point() else t.cpu().numpy()
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_build_steps_match_oracle(case):
+    import cluster_indexed_sparse_wi_b300 as wl
+    c, g, cfg = make(case)
+    Kf, Vf = f64(g["K"]), f64(g["V"])
+    K, V = bf16_tensor(g["K"], "cuda"), bf16_tensor(g["V"], "cuda")
+    ix = wl.WaveIndex(cfg, "cuda")
+    ix.init(K)
+    torch.cuda.synchronize()
+    B, H, N, k = c["B"], c["Hkv"], c["N"], c["k"]
+    norms = ix.workspace[256:256 + B * H * N * 4].view(torch.float32).view(B, H, N)
+    np.testing.assert_allclose(dl(norms), np.linalg.norm(Kf, axis=-1), rtol=1e-6)
+    segs = seg_positions(cfg)
+    asg = dl(ix.assign)
+    steady = np.ones(N, bool)
+    steady[c["sink"]:N - c["window"]] = False
+    assert np.all(asg[:, :, steady] == -1)
+    mu = dl(ix.unit_centroid)
+    for b in range(B):
+        for h in range(H):
+            for s, pos in enumerate(segs):
+                ref = wi.kmeans_init(Kf[b, h][pos], k)
+                assert ulp_ok(mu[b, h, s * k:(s + 1) * k], ref).all()
+    ties = 0
+    for it in range(c["iters"]):
+        mu_in = dl(ix.unit_centroid)
+        ix.assign_step(K)
+        torch.cuda.synchronize()
+        a = dl(ix.assign)
+        for b in range(B):
+            for h in range(H):
+                for s, pos in enumerate(segs):
+                    if pos.size == 0:
+                        continue
+                    a_ref, cos = wi.kmeans_assign(Kf[b, h][pos], mu_in[b, h, s * k:(s + 1) * k])
+                    a_gpu = a[b, h][pos] - s * k
+                    assert np.all((a_gpu >= 0) & (a_gpu < k))
+                    bad = np.nonzero(a_gpu != a_ref)[0]
+                    gap = np.abs(cos[bad, a_gpu[bad]] - cos[bad, a_ref[bad]])
+                    assert np.all(gap < COS_TIE), (it, b, h, s, gap.max(initial=0))
+                    ties += bad.size
+        ix.update_step(K)
+        torch.cuda.synchronize()
+        assert ix.status() == 0
+        mu_out = dl(ix.unit_centroid)
+        for b in range(B):
+            for h in range(H):
+                P = np.arange(c["sink"], N - c["window"])
+                st = wi.index_statistics(Kf[b, h], Vf[b, h], P, a[b, h][P], cfg.n_clusters)
+                assert np.array_equal(dl(ix.size)[b, h], st["size"])
+                assert np.array_equal(dl(ix.offset)[b, h], st["offset"])
+                assert np.array_equal(dl(ix.perm)[b, h], st["perm"])
+                for s, pos in enumerate(segs):
+                    if pos.size == 0:
+                        continue
+                    ref, _ = wi.kmeans_update(Kf[b, h][pos], a[b, h][pos] - s * k,
+                                              mu_in[b, h, s * k:(s + 1) * k])
+                    ok = ulp_ok(mu_out[b, h, s * k:(s + 1) * k], ref)
+                    assert ok.all(), (it, b, h, s, np.argwhere(~ok)[:5])
+    ix.finalize(K, V)
+    torch.cuda.synchronize()
+    assert ix.status() == 0
+    a = dl(ix.assign)
+    for b in range(B):
+        for h in range(H):
+            P = np.arange(c["sink"], N - c["window"])
+            st = wi.index_statistics(Kf[b, h], Vf[b, h], P, a[b, h][P], cfg.n_clusters)
+            for name in ("centroid_key", "value_sum"):
+                got = dl(ix.tensors[name])[b, h]
+                scale = np.abs(st[name]).max(axis=1, keepdims=True) + 1e-6
+                assert np.all(np.abs(got - st[name]) <= 1e-5 * scale), name
+            assert np.array_equal(dl(ix.k_sorted)[b, h], st["k_sorted"])
+            assert np.array_equal(dl(ix.v_sorted)[b, h], st["v_sorted"])
+    print("assignment ties resolved differently:", ties)
+
+
+@pytest.mark.parametrize("case", ["tiny_4k_1h", "multi_seg_ragged"])
+def test_fused_build_equals_steps_and_tracks_oracle(case):
+    import cluster_indexed_sparse_wi_b300 as wl
+    c, g, cfg = make(case, seed=9)
+    K, V = bf16_tensor(g["K"], "cuda"), bf16_tensor(g["V"], "cuda")
+    ix1 = wl.WaveIndex(cfg, "cuda").build(K, V)
+    ix2 = wl.WaveIndex(cfg, "cuda")
+    ix2.init(K)
+    for _ in range(c["iters"]):
+        ix2.assign_step(K)
+        ix2.update_step(K)
+    ix2.finalize(K, V)
+    torch.cuda.synchronize()
+    for name in ix1.tensors:
+        assert torch.equal(ix1.tensors[name], ix2.tensors[name]), name
+    # end to end against the oracle build
+    oidx = wi.build_index(f64(g["K"]), f64(g["V"]), c["sink"], c["window"], c["seg_len"], c["k"],
+                          c["iters"])
+    a_gpu = dl(ix1.assign)
+    agree = float(np.mean(a_gpu == oidx["assign"]))
+    print("end-to-end assignment agreement", agree)
+    assert agree >= 0.999
+
+
+def test_bad_assignment_reports_status_not_fault():
+    import cluster_indexed_sparse_wi_b300 as wl
+    c, g, cfg = make("k100_short_tail")
+    K = bf16_tensor(g["K"], "cuda")
+    ix = wl.WaveIndex(cfg, "cuda")
+    ix.init(K)
+    ix.assign_step(K)
+    torch.cuda.synchronize()
+    ix.assign[0, 0, 100] = cfg.n_clusters + 5  # not an id of position 100's segment
+    ix.update_step(K)
+    assert ix.status() == wl._lib.WI_ERR_INDEX_MISMATCH
+    assert ix.status() == 0  # read-and-clear
+    ix.assign_step(K)
+    ix.update_step(K)
+    assert ix.status() == 0
