@@ -8,7 +8,9 @@ Inference" (technical summary §2.A wave index, §3 segmented clustering).
 
 from . import _lib  # noqa: F401
 from .api import (  # noqa: F401
+    DecodeStep,
     Decoder,
+    capture_graph,
     IndexConfig,
     WaveIndex,
     build_index,

@@ -97,7 +97,10 @@ class WaveIndex:
 
     def __init__(self, cfg: IndexConfig, device):
         self.cfg = cfg
-        self.device = torch.device(device)
+        dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
         B, H, N, C, d, n = cfg.B, cfg.Hkv, cfg.N, cfg.n_clusters, cfg.d, cfg.n_idx
         shapes = {
             "centroid_key": (B, H, C, d), "unit_centroid": (B, H, C, d),
@@ -212,6 +215,10 @@ class Decoder:
         c = self.index.cfg
         _need(q, "q", torch.bfloat16, (c.B, self.Hq, c.d), self.index.device)
 
+    def capture(self, q, K, V, with_topk: bool = False) -> "torch.cuda.CUDAGraph":
+        """The fused decode call on device buffers, captured as a CUDA graph."""
+        return capture_graph(lambda: self(q, K, V, with_topk=with_topk), self.index.device)
+
     def __call__(self, q, K, V, stream=None, with_topk: bool = True):
         """out [B,Hq,128] f32, lse [B,Hq] f32, topk ids [B,Hq,r] i32."""
         self._q(q)
@@ -276,6 +283,54 @@ class Decoder:
 
     def status(self, stream=None) -> int:
         return sync_status(self.workspace, stream)
+
+
+def capture_graph(fn, device) -> "torch.cuda.CUDAGraph":
+    """Run `fn` once on a side stream (first-call set-up), then capture it into
+    a CUDA graph; replaying the graph re-issues the same kernel launches with
+    one host call."""
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        fn()
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    return g
+
+
+class DecodeStep:
+    """One decode step as a CUDA graph over host buffers: q is copied from
+    pinned host memory, the four decode kernels run, and out / lse are copied
+    back into pinned host memory.  `step(q_host)` replays the graph and waits
+    for the results."""
+
+    def __init__(self, dec: "Decoder", K, V):
+        c = dec.index.cfg
+        dev = dec.index.device
+        self.dec = dec
+        self.q_host = torch.zeros((c.B, dec.Hq, c.d), dtype=torch.bfloat16, pin_memory=True)
+        self.out_host = torch.empty(tuple(dec.out.shape), dtype=torch.float32, pin_memory=True)
+        self.lse_host = torch.empty(tuple(dec.lse.shape), dtype=torch.float32, pin_memory=True)
+        self.q_dev = torch.zeros((c.B, dec.Hq, c.d), dtype=torch.bfloat16, device=dev)
+        self.h2d_bytes = self.q_host.numel() * 2
+        self.d2h_bytes = self.out_host.numel() * 4 + self.lse_host.numel() * 4
+
+        def body():
+            self.q_dev.copy_(self.q_host, non_blocking=True)
+            dec(self.q_dev, K, V, with_topk=False)
+            self.out_host.copy_(dec.out, non_blocking=True)
+            self.lse_host.copy_(dec.lse, non_blocking=True)
+
+        self.graph = capture_graph(body, dev)
+
+    def __call__(self, q_host: Optional[torch.Tensor] = None):
+        if q_host is not None:
+            self.q_host.copy_(q_host)
+        self.graph.replay()
+        torch.cuda.current_stream().synchronize()
+        return self.out_host, self.lse_host
 
 
 def decode_attention(q, K, V, index: WaveIndex, r: int, scale: Optional[float] = None,

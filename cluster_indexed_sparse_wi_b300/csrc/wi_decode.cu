@@ -23,6 +23,7 @@
 // every exponential is an exp2.
 #include <float.h>
 #include <limits.h>
+#include <stddef.h>
 
 #include "wi_device.cuh"
 #include "wi_internal.h"
@@ -328,19 +329,22 @@ constexpr int kStages = 2;
 constexpr int kWinCap = 512;   // retrieved clusters staged per window
 
 struct __align__(128) AttSmem {
-  uint16_t k[kStages][kTile * kD];
+  uint16_t k[kStages][kTile * kD];  // bulk-copy destinations: 16-byte aligned
   uint16_t v[kStages][kTile * kD];
-  int win_prefix[kWinCap + 1];
-  int win_row[kWinCap];
-  float red_o[kAttWarps][kD];
+  float red_o[kAttWarps][kD];       // written as float4: 16-byte aligned
   float red_m[kAttWarps];
   float red_l[kAttWarps];
-  unsigned long long bar[kStages];
+  unsigned long long bar[kStages];  // mbarriers: 8-byte aligned
+  int win_prefix[kWinCap + 1];
+  int win_row[kWinCap];
 };
+static_assert(offsetof(AttSmem, v) % 128 == 0, "staging buffer alignment");
+static_assert(offsetof(AttSmem, red_o) % 16 == 0, "float4 reduction buffer alignment");
+static_assert(offsetof(AttSmem, bar) % 8 == 0, "mbarrier alignment");
 
 template <int G>
 struct EstSmem {
-  float red_o[kAttWarps][G][kD];
+  float red_o[kAttWarps][G][kD];  // offset 0, written as float4
   float red_l[kAttWarps][G];
 };
 

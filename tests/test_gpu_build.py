@@ -2,7 +2,8 @@
 each step takes the GPU's own previous state as the oracle's input, so a
 rounding difference in one iteration does not cascade into the next.
 
-Rules: key norms rel 1e-6; centroids within 1 bf16 ulp per component;
+Rules: key norms rel 1e-6; centroids within 1 bf16 ulp per component plus the
+f32 summation bound n_c 2^-24 / ||sum|| (components that cancel to near zero);
 assignments bit-exact except where the oracle's cosines of the two choices
 differ by less than 1e-5 (a tie); size / offset / perm bit-exact; mean keys and
 value sums within 1e-5 of the row's scale; sorted K/V copies bit-exact.
@@ -42,10 +43,23 @@ def make(case, seed=5):
     return c, g, cfg
 
 
-def ulp_ok(a, b):
+def ulp_ok(a, b, atol=0.0):
     m = np.maximum(np.abs(a), np.abs(b))
     ulp = np.where(m > 0, 2.0 ** (np.floor(np.log2(np.where(m > 0, m, 1.0))) - 7), 0.0)
-    return np.abs(a - b) <= ulp + 1e-30
+    return np.abs(a - b) <= ulp + atol + 1e-30
+
+
+def update_atol(keys, a_local, k):
+    """Per-centroid bound on the f32 error of normalize(sum k_i/||k_i||): each
+    of the n_c unit-vector terms adds at most 2^-24 per component to the sum
+    (plus the normalisation's own rounding), so a component that cancels to
+    near zero may differ by n_c 2^-24 / ||S_c|| beyond one bf16 ulp."""
+    unit = keys / np.linalg.norm(keys, axis=1, keepdims=True)
+    S = np.zeros((k, keys.shape[1]))
+    np.add.at(S, a_local, unit)
+    n = np.bincount(a_local, minlength=k)
+    nrm = np.linalg.norm(S, axis=1)
+    return (4.0 * (n + 2) * 2.0 ** -24 / np.where(nrm > 0, nrm, 1.0))[:, None]
 
 
 def seg_positions(cfg):
@@ -113,7 +127,8 @@ def test_build_steps_match_oracle(case):
                         continue
                     ref, _ = wi.kmeans_update(Kf[b, h][pos], a[b, h][pos] - s * k,
                                               mu_in[b, h, s * k:(s + 1) * k])
-                    ok = ulp_ok(mu_out[b, h, s * k:(s + 1) * k], ref)
+                    tol = update_atol(Kf[b, h][pos], a[b, h][pos] - s * k, k)
+                    ok = ulp_ok(mu_out[b, h, s * k:(s + 1) * k], ref, tol)
                     assert ok.all(), (it, b, h, s, np.argwhere(~ok)[:5])
     ix.finalize(K, V)
     torch.cuda.synchronize()

@@ -241,3 +241,22 @@ def test_bounded_wait_timeout_reports_status_and_context_survives():
     out = dec(q, K, V)[0]
     assert dec.status() == 0
     assert torch.equal(out, ref)
+
+
+def test_graph_replay_and_host_step_match_direct_call():
+    g, oidx = random_case(29, B=1, Hq=8, Hkv=2, N=9000, sink=4, window=128, seg_len=4096, k=64)
+    ix = gpu_index(g, oidx, 4, 128, 4096, 64)
+    wl = lib()
+    K, V, q = (bf16_tensor(g[n], "cuda") for n in ("K", "V", "q"))
+    dec = wl.Decoder(ix, 8, 12)
+    out, lse, _ = dec(q, K, V)
+    ref_out, ref_lse = out.clone(), lse.clone()
+    gr = dec.capture(q, K, V)
+    dec.out.zero_()
+    gr.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dec.out, ref_out)
+    step = wl.DecodeStep(dec, K, V)
+    out_h, lse_h = step(q.cpu())
+    assert torch.equal(out_h, ref_out.cpu()) and torch.equal(lse_h, ref_lse.cpu())
+    assert dec.status() == 0
