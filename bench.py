@@ -266,12 +266,26 @@ def run_reference(args, w, r):
     print(json.dumps(line), flush=True)
 
 
+def replica_workload(w, rank):
+    """Rank `rank`'s replica of the workload: the same shapes over its own
+    sequences (weak scaling; ranks share no data)."""
+    return w if rank == 0 else w.replace(seeds=tuple(s + 100003 * rank for s in w.seeds))
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings (the only collective: timing)."""
+    import torch
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def workload_config(w, r):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
             "clusters_per_head": w.n_clusters, "seg_len": w.seg_len, "k_per_seg": w.k_per_seg,
             "kmeans_iters": w.iters, "sink": w.sink, "window": w.window, "r": r,
             "l2": "flushed between timed steps (256 MiB write)",
-            "step": "decode (score, select, attend+estimate, merge) over an index built in the "
+            "step": "decode (score; select + estimate; attend + merge) over an index built in the "
                     "same run; build timed separately under 'build'"}
 
 
@@ -300,7 +314,7 @@ def main():
 
     # per-rank replica: own sequences (weak scaling), no data-path collective
     t0 = time.perf_counter()
-    wr = w if rank == 0 else w.replace(seeds=tuple(s + 100003 * rank for s in w.seeds))
+    wr = replica_workload(w, rank)
     g_np = generate(wr)
     t_gen = time.perf_counter() - t0
 
@@ -351,8 +365,7 @@ def main():
     # and the events time the GPU work alone.
     g_step = dec.capture(q, K, V)
     g_stage = [wl.capture_graph(fn, dev) for fn in (
-        lambda: dec.score(q), lambda: dec.select(), lambda: dec.attend(q, K, V),
-        lambda: dec.merge())]
+        lambda: dec.score(q), lambda: dec.select(), lambda: dec.attend(q, K, V))]
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         g_step.replay()
@@ -380,8 +393,8 @@ def main():
 
     # ---- timed region 2: the same step as its four stage calls, for the
     # per-kernel durations of the roofline
-    names = ["score", "select", "attend", "merge"]
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    names = ["score", "select", "attend"]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
         e = kev[i]
@@ -420,21 +433,18 @@ def main():
     steady_bytes = w.B * w.Hkv * (w.sink + w.window) * w.d * 2 * 2
     retr_bytes = retrieved_unique_bytes(dec.topk[..., :r].contiguous(), n_size, w.Hq // w.Hkv)
     step_bytes = kbar_bytes + vsum_bytes + steady_bytes + retr_bytes
-    kern_bytes = {"score": kbar_bytes, "select": 0, "attend": vsum_bytes + steady_bytes + retr_bytes,
-                  "merge": 0}
+    # select's second role streams the value sums (estimate of every cluster)
+    kern_bytes = {"score": kbar_bytes, "select": vsum_bytes, "attend": steady_bytes + retr_bytes}
 
     ms = statistics.mean(step_ms)
+    e2e_mean = statistics.mean(e2e_ms)
     if ws > 1:
-        t = torch.tensor([ms, statistics.mean(e2e_ms)], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_mean = t.tolist()
-    else:
-        e2e_mean = statistics.mean(e2e_ms)
+        ms, e2e_mean = max_over_ranks([ms, e2e_mean], dist, dev)
     queries = w.B * ws
     value = queries / (ms * 1e-3)
 
-    # dominant HBM-bound kernel (select and merge move no algorithmic HBM bytes)
-    dom = max(("score", "attend"), key=lambda n: kern_ms[n])
+    # dominant kernel by time (all three stream algorithmic bytes from HBM)
+    dom = max(names, key=lambda n: kern_ms[n])
     hbm_peak = float(pk["hbm_gbs"])
     ach = kern_bytes[dom] / (kern_ms[dom] * 1e-3) / 1e9 if kern_bytes[dom] else 0.0
     roofline = {"kernel": dom + "_kernel", "bound": "hbm", "achieved": ach, "peak": hbm_peak,
@@ -476,7 +486,7 @@ def main():
                 "how": "DecodeStep graph: H2D q (pinned), 4 kernels, D2H out+lse (pinned), "
                        "host waits; wall clock per step (q copied into the pinned buffer "
                        "inside the timed region)"},
-        "gpu_launches": 4 * args.steps * 2,
+        "gpu_launches": 3 * args.steps * 2,
         "timing": "CUDA events around CUDA-graph replays of the decode call; L2 flushed "
                   "before every step outside the events",
         "clocks": clocks,

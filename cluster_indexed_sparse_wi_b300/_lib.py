@@ -32,7 +32,7 @@ SYMBOLS = [
     "wi_index_sizes", "wi_build_workspace_bytes", "wi_build_index", "wi_build_init",
     "wi_kmeans_assign", "wi_kmeans_update", "wi_build_finalize", "wi_decode_workspace_bytes",
     "wi_decode_workspace_layout", "wi_decode_attention", "wi_decode_score", "wi_decode_select",
-    "wi_decode_attend", "wi_decode_merge", "wi_sync_status", "wi_status_string", "wi_debug_inject",
+    "wi_decode_attend", "wi_sync_status", "wi_status_string", "wi_debug_inject",
     "wi_version",
 ]
 
@@ -64,7 +64,7 @@ class IndexStruct(ctypes.Structure):
 
 class DecodeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("scores", "head_max", "selected", "sel_prefix", "sel_mask", "att_partials",
+                ("scores", "head_max", "selected", "sel_prefix", "counters", "att_partials",
                  "est_partials", "total")] + [
         (n, ctypes.c_int) for n in ("att_splits", "est_chunks", "est_chunk_clusters", "reserved")]
 
@@ -98,8 +98,7 @@ def lib() -> ctypes.CDLL:
         "wi_decode_attention": (i, [dp, vp, vp, vp, ip, vp, vp, vp, vp, sz, vp]),
         "wi_decode_score": (i, [dp, vp, ip, vp, sz, vp]),
         "wi_decode_select": (i, [dp, ip, vp, vp, sz, vp]),
-        "wi_decode_attend": (i, [dp, vp, vp, vp, ip, vp, sz, vp]),
-        "wi_decode_merge": (i, [dp, ip, vp, vp, vp, sz, vp]),
+        "wi_decode_attend": (i, [dp, vp, vp, vp, ip, vp, vp, vp, sz, vp]),
         "wi_sync_status": (i, [vp, vp, P(i)]),
         "wi_status_string": (ctypes.c_char_p, [i]),
         "wi_debug_inject": (i, [i]),

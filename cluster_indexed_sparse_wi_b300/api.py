@@ -245,18 +245,15 @@ class Decoder:
                                          _stream(stream)), "wi_decode_select")
 
     def attend(self, q, K, V, stream=None):
+        """Exact attention, retrieved-estimate subtraction and merge into
+        self.out / self.lse."""
         self._q(q)
         self.index._kv(K, V)
         L.check(L.lib().wi_decode_attend(ctypes.byref(self.params), _ptr(q), _ptr(K), _ptr(V),
-                                         ctypes.byref(self.index.struct), _ptr(self.workspace),
+                                         ctypes.byref(self.index.struct), _ptr(self.out),
+                                         _ptr(self.lse), _ptr(self.workspace),
                                          self.workspace.numel(), _stream(stream)),
                 "wi_decode_attend")
-
-    def merge(self, stream=None):
-        L.check(L.lib().wi_decode_merge(ctypes.byref(self.params), ctypes.byref(self.index.struct),
-                                        _ptr(self.out), _ptr(self.lse), _ptr(self.workspace),
-                                        self.workspace.numel(), _stream(stream)),
-                "wi_decode_merge")
         return self.out, self.lse
 
     # workspace views ------------------------------------------------------

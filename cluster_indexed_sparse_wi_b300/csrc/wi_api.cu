@@ -173,10 +173,9 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   if (splits > 128) splits = 128;
   if (splits < 1) splits = 1;
   L->att_splits = (int)splits;
-  L->est_chunk_clusters = 256;
+  L->est_chunk_clusters = wi::kEstChunk;
   L->est_chunks = (C + L->est_chunk_clusters - 1) / L->est_chunk_clusters;
   const int r_slots = p->r > 0 ? p->r : 1;
-  const int n_words = (C + 31) / 32;
   size_t off = kStatusBytes;
   L->scores = off;
   off += align256((size_t)heads * C * 4);
@@ -186,10 +185,10 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   off += align256((size_t)heads * r_slots * 4);
   L->sel_prefix = off;
   off += align256((size_t)heads * (p->r + 1) * 4);
-  L->sel_mask = off;
-  off += align256((size_t)heads * n_words * 4);
+  L->counters = off;
+  off += align256((size_t)heads * 4);
   L->att_partials = off;
-  off += align256((size_t)heads * L->att_splits * wi::kPartStride * 4);
+  off += align256((size_t)heads * L->att_splits * 2 * wi::kPartStride * 4);
   L->est_partials = off;
   off += align256((size_t)heads * L->est_chunks * wi::kPartStride * 4);
   L->total = off;
@@ -231,7 +230,6 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->r = p->r;
   a->C = ix->n_clusters;
   a->N_idx = p->N - p->sink - p->window;
-  a->n_words = (a->C + 31) / 32;
   a->scale = p->scale;
   a->q = static_cast<const uint16_t*>(q);
   a->K = static_cast<const uint16_t*>(K);
@@ -247,7 +245,7 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->head_max = reinterpret_cast<float*>(w + L.head_max);
   a->sel_ids = reinterpret_cast<int*>(w + L.selected);
   a->sel_prefix = reinterpret_cast<int*>(w + L.sel_prefix);
-  a->sel_mask = reinterpret_cast<uint32_t*>(w + L.sel_mask);
+  a->counters = reinterpret_cast<int*>(w + L.counters);
   a->att_part = reinterpret_cast<float*>(w + L.att_partials);
   a->est_part = reinterpret_cast<float*>(w + L.est_partials);
   a->att_splits = L.att_splits;
@@ -388,27 +386,17 @@ int wi_decode_select(const wi_decode_params* p, const wi_index* index, int32_t* 
 }
 
 int wi_decode_attend(const wi_decode_params* p, const void* q, const void* K, const void* V,
-                     const wi_index* index, void* workspace, size_t workspace_bytes,
-                     wi_stream_t stream) {
+                     const wi_index* index, float* out, float* lse, void* workspace,
+                     size_t workspace_bytes, wi_stream_t stream) {
   DecodeArgs a;
   int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, true);
-  if (st != WI_OK) return st;
-  if ((st = device_ok()) != WI_OK) return st;
-  a.inject = g_inject.exchange(0);
-  return cuda_status(wi::launch_decode_attend(a, (cudaStream_t)stream));
-}
-
-int wi_decode_merge(const wi_decode_params* p, const wi_index* index, float* out, float* lse,
-                    void* workspace, size_t workspace_bytes, wi_stream_t stream) {
-  DecodeArgs a;
-  int st = fill_decode_args(p, nullptr, nullptr, nullptr, index, workspace, workspace_bytes, &a,
-                            false);
   if (st != WI_OK) return st;
   if (out == nullptr) return WI_ERR_INVALID_ARG;
   if ((st = device_ok()) != WI_OK) return st;
   a.out = out;
   a.lse = lse;
-  return cuda_status(wi::launch_decode_merge(a, (cudaStream_t)stream));
+  a.inject = g_inject.exchange(0);
+  return cuda_status(wi::launch_decode_attend(a, (cudaStream_t)stream));
 }
 
 int wi_decode_attention(const wi_decode_params* p, const void* q, const void* K, const void* V,
@@ -427,7 +415,6 @@ int wi_decode_attention(const wi_decode_params* p, const void* q, const void* K,
   cudaError_t e = wi::launch_decode_score(a, s);
   if (e == cudaSuccess) e = wi::launch_decode_select(a, s);
   if (e == cudaSuccess) e = wi::launch_decode_attend(a, s);
-  if (e == cudaSuccess) e = wi::launch_decode_merge(a, s);
   return cuda_status(e);
 }
 

@@ -1,24 +1,27 @@
 // Decode kernels of the wave-index tripartite attention ("RetroInfer: A Vector
 // Storage Engine for Scalable Long-Context LLM Inference", technical summary
-// §2.A: steady zone, retrieval zone, estimation zone; (ar) §2.a: estimation
-// from centroids and the value sum; (ar) §2.b: contiguous retrieved KV).
+// (es) §2.A: steady zone, retrieval zone, estimation zone; technical summary
+// (ar) §2.a: estimation from centroids and the value sum, §2.b: retrieved KV
+// laid out contiguously).  Three launches, chained with programmatic
+// dependent launch:
 //
-//   score_kernel   : s[b,h,c] = scale q_h . kbar_c (-inf if empty); one pass
-//                    over the f32 centroid keys, one warp per 512-byte row,
-//                    128-bit loads, all query heads of a KV group per pass.
-//   select_kernel  : per query head, radix select of the r largest scores
-//                    (composite order: score desc, id asc), selected ids in
-//                    ascending order, their token prefix and a bit mask.
-//   attend_kernel  : one launch, two block roles.
-//                    (a) exact attention over the steady zone and the
-//                        retrieved clusters: token-balanced splits, rows
-//                        staged into shared memory by the TMA bulk-copy engine
-//                        (cp.async.bulk + mbarrier, double buffered), warp
-//                        shuffle dot products, online softmax -> (m, l, o).
-//                    (b) estimation zone over cluster chunks of one KV head:
-//                        every non-retrieved non-empty cluster adds
-//                        n_c e^{s_c - m} to l and e^{s_c - m} vsum_c to o.
-//   merge_kernel   : log-sum-exp merge of all partials -> out, lse.
+//   score_kernel   s[b,h,c] = scale q_h . kbar_c (-inf if empty): one pass over
+//                  the f32 centroid keys, one warp per 512-byte row, 128-bit
+//                  loads, all query heads of a KV group per pass.
+//   select_kernel  two block roles in one launch, so that the selection's
+//                  latency hides under the value-sum stream:
+//                  (a) per query head, radix select of the r largest scores
+//                      (order: score desc, id asc): ids ascending + token prefix;
+//                  (b) per chunk of clusters of one KV head, the estimate of
+//                      EVERY non-empty cluster: (m, l = sum n_c e^{s_c-m},
+//                      o = sum e^{s_c-m} vsum_c).
+//   attend_kernel  per (query head, split of its token list): exact attention
+//                  over the steady zone and the retrieved clusters, rows staged
+//                  into shared memory by the TMA bulk-copy engine (cp.async.bulk
+//                  + mbarrier, double buffered); the same block emits the
+//                  retrieved clusters' estimates with a negative sign, so that
+//                  all-minus-retrieved is the estimation zone; the last block of
+//                  a head merges every partial (log-sum-exp) into out and lse.
 // Softmax quantities are kept in log2 units (logits scaled by log2 e) so that
 // every exponential is an exp2.
 #include <float.h>
@@ -52,13 +55,15 @@ cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 // K1: centroid scoring
 // --------------------------------------------------------------------------
 constexpr int kScoreThreads = 256;
+constexpr int kScoreWarps = kScoreThreads / 32;
 
 template <int G>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(DecodeArgs a, int rows_per_block,
                                                               int blocks_per_head) {
   grid_dep_launch();
   grid_dep_wait();
-  constexpr int ROWS = 32 / G;
+  constexpr int ROWS = 32 / G;  // rows per transpose-reduce batch
+  constexpr int NB = ROWS >= 16 ? 1 : 2;  // batches in flight: 8-32 rows per warp
   const int bg = blockIdx.x / blocks_per_head;
   const int chunk = blockIdx.x - bg * blocks_per_head;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
@@ -76,41 +81,49 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(DecodeArgs a, int 
   const int* sz = a.size + (size_t)bg * a.C;
   const int c_begin = chunk * rows_per_block;
   const int c_end = min(a.C, c_begin + rows_per_block);
-  constexpr int kWarps = kScoreThreads / 32;
-  for (int c0 = c_begin + warp * ROWS; c0 < c_end; c0 += kWarps * ROWS) {
-    float4 kv[ROWS];
+  for (int c0 = c_begin + warp * NB * ROWS; c0 < c_end; c0 += kScoreWarps * NB * ROWS) {
+    float4 kv[NB * ROWS];
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) {
+    for (int r = 0; r < NB * ROWS; ++r) {
       const int c = c0 + r;
-      kv[r] = (c < c_end) ? __ldg(kb + (size_t)c * (kD / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      kv[r] = (c < c_end) ? __ldg(kb + (size_t)c * (kD / 4) + lane)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float v[32];
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r)
+    for (int nb = 0; nb < NB; ++nb) {
+      float v[32];
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        v[r * G + h] = kv[r].x * qv[h].x + kv[r].y * qv[h].y + kv[r].z * qv[h].z + kv[r].w * qv[h].w;
-    const float tot = warp_transpose_sum32(v, lane);
-    const int r = lane / G, h = lane - (lane / G) * G;
-    const int c = c0 + r;
-    if (c < c_end) {
-      const int n = __ldg(sz + c);
-      a.scores[((size_t)b * a.Hq + g * G + h) * a.C + c] = n > 0 ? tot : -INFINITY;
+      for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 k4 = kv[nb * ROWS + r];
+          v[r * G + h] = k4.x * qv[h].x + k4.y * qv[h].y + k4.z * qv[h].z + k4.w * qv[h].w;
+        }
+      const float tot = warp_transpose_sum32(v, lane);
+      const int r = lane / G, h = lane - (lane / G) * G;
+      const int c = c0 + nb * ROWS + r;
+      if (c < c_end) {
+        const int n = __ldg(sz + c);
+        a.scores[((size_t)b * a.Hq + g * G + h) * a.C + c] = n > 0 ? tot : -INFINITY;
+      }
     }
   }
 }
 
 // --------------------------------------------------------------------------
-// K2: per-head top-r radix select
+// K2: selection (role a) and estimation over all clusters (role b)
 // --------------------------------------------------------------------------
-constexpr int kSelThreads = 1024;
-constexpr int kSelCacheMax = 32768;  // keys kept in shared memory up to this C
+constexpr int kK2Threads = 512;
+constexpr int kK2Warps = kK2Threads / 32;
+constexpr int kSelCacheMax = 16384;              // keys kept in shared memory up to this C
+constexpr int kEstBatch = kEstChunk / kK2Warps;  // clusters per warp: 16
+static_assert(kEstBatch == 16, "estimation batch layout");
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   return (s == -INFINITY) ? 0u : float_key(s);  // 0 <=> empty cluster
 }
 
-// Exclusive scan of an int pair over the block; returns the prefix, and the
+// Exclusive scan of an int pair over the block; returns the prefix and the
 // block total in *total.  sh must hold 33 entries.
 __device__ __forceinline__ int2 block_scan2(int2 v, int2* sh, int2* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -150,26 +163,30 @@ __device__ __forceinline__ int2 block_scan2(int2 v, int2* sh, int2* total) {
   return res;
 }
 
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(DecodeArgs a, int cached) {
-  extern __shared__ __align__(16) uint32_t skey[];
-  __shared__ int hist[256];
-  __shared__ int2 sh_scan[33];
-  __shared__ int sh_i[8];
-  __shared__ uint32_t sh_u[32];
-  grid_dep_launch();
-  grid_dep_wait();
+struct SelShared {
+  int hist[256];
+  int2 scan[33];
+  int i[8];
+  uint32_t u[32];
+};
+
+// Role (a): the r_eff = min(r, non-empty) largest scores of one query head.
+// Radix select on order-preserving keys, 8 bits per pass, histograms built
+// with warp-aggregated shared atomics; stops as soon as the boundary bin is
+// taken whole.  Equal keys at the boundary keep the lowest ids.
+__device__ void select_head(const DecodeArgs& a, int bh, uint32_t* skey, SelShared& S,
+                            int cached) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bh = blockIdx.x, b = bh / a.Hq, h = bh - b * a.Hq, g = h / a.G;
+  const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / a.G;
   const int C = a.C;
   const float* sc = a.scores + (size_t)bh * C;
   const int* sz = a.size + ((size_t)b * a.Hkv + g) * C;
-  auto key = [&](int c) -> uint32_t { return cached ? skey[c] : score_key(sc[c]); };
+  auto key = [&](int c) -> uint32_t { return cached ? skey[c] : score_key(__ldcg(sc + c)); };
 
-  // pass 0: keys, number of non-empty clusters, maximum
   int valid = 0;
   uint32_t kmax = 0;
-  for (int c = tid; c < C; c += kSelThreads) {
-    const uint32_t k = score_key(sc[c]);
+  for (int c = tid; c < C; c += kK2Threads) {
+    const uint32_t k = score_key(__ldcg(sc + c));
     if (cached) skey[c] = k;
     valid += (k != 0);
     kmax = max(kmax, k);
@@ -180,41 +197,44 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(DecodeArgs a, in
     kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
   }
   if (lane == 0) {
-    sh_scan[warp].x = valid;
-    sh_u[warp] = kmax;
+    S.scan[warp].x = valid;
+    S.u[warp] = kmax;
   }
   __syncthreads();
   if (warp == 0) {
-    int v = sh_scan[lane].x;
-    uint32_t m = sh_u[lane];
+    int v = lane < kK2Warps ? S.scan[lane].x : 0;
+    uint32_t m = lane < kK2Warps ? S.u[lane] : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       v += __shfl_xor_sync(kFull, v, o);
       m = max(m, __shfl_xor_sync(kFull, m, o));
     }
     if (lane == 0) {
-      sh_i[0] = v;
-      sh_i[5] = (int)m;
+      S.i[0] = v;
+      S.i[5] = (int)m;
     }
   }
   __syncthreads();
-  valid = sh_i[0];
-  kmax = (uint32_t)sh_i[5];
+  valid = S.i[0];
+  kmax = (uint32_t)S.i[5];
   const int r = a.r;
   const int r_eff = min(r, valid);
   if (tid == 0) a.head_max[bh] = valid > 0 ? key_float(kmax) : -INFINITY;
 
-  // radix select of the r_eff-th largest key, 8 bits per pass
   uint32_t prefix = 0, mask = 0;
-  int remaining = r_eff, count_eq = 0;
+  int remaining = r_eff, count = 0;
   if (r_eff > 0) {
 #pragma unroll 1
     for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) hist[tid] = 0;
+      if (tid < 256) S.hist[tid] = 0;
       __syncthreads();
-      for (int c = tid; c < C; c += kSelThreads) {
-        const uint32_t k = key(c);
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xffu], 1);
+      for (int base = 0; base < C; base += kK2Threads) {
+        const int c = base + tid;
+        const uint32_t k = c < C ? key(c) : 0u;
+        const bool in = k != 0u && (k & mask) == prefix;
+        const int d = in ? (int)((k >> shift) & 0xffu) : 256 + lane;
+        const unsigned peers = __match_any_sync(kFull, d);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&S.hist[d], __popc(peers));
       }
       __syncthreads();
       if (warp == 0) {
@@ -222,7 +242,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(DecodeArgs a, in
         int tot = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          cnt[j] = hist[255 - 8 * lane - j];
+          cnt[j] = S.hist[255 - 8 * lane - j];
           tot += cnt[j];
         }
         int incl = tot;
@@ -237,9 +257,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(DecodeArgs a, in
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (acc + cnt[j] >= remaining) {
-              sh_i[1] = 255 - 8 * lane - j;
-              sh_i[2] = acc;
-              sh_i[3] = cnt[j];
+              S.i[1] = 255 - 8 * lane - j;
+              S.i[2] = acc;
+              S.i[3] = cnt[j];
               break;
             }
             acc += cnt[j];
@@ -247,47 +267,49 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(DecodeArgs a, in
         }
       }
       __syncthreads();
-      remaining -= sh_i[2];
-      count_eq = sh_i[3];
-      prefix |= (uint32_t)sh_i[1] << shift;
+      remaining -= S.i[2];
+      count = S.i[3];
+      prefix |= (uint32_t)S.i[1] << shift;
       mask |= 0xffu << shift;
+      if (count == remaining) break;  // the whole boundary bin is selected
     }
   }
   const bool any = r_eff > 0;
-  const uint32_t T = prefix;  // the r_eff-th largest key
-  // equal keys at the threshold: keep the `remaining` lowest ids
+  const bool tie_cut = any && remaining < count;  // equal full keys at the boundary
   int c_cut = INT_MAX;
-  const int per = (C + kSelThreads - 1) / kSelThreads;
+  const int per = (C + kK2Threads - 1) / kK2Threads;
   const int my0 = min(C, tid * per), my1 = min(C, my0 + per);
-  if (any && remaining < count_eq) {
+  if (tie_cut) {
     int ne = 0;
-    for (int c = my0; c < my1; ++c) ne += (key(c) == T);
+    for (int c = my0; c < my1; ++c) ne += (key(c) == prefix);
     int2 tot;
-    const int before = block_scan2(make_int2(ne, 0), sh_scan, &tot).x;
+    const int before = block_scan2(make_int2(ne, 0), S.scan, &tot).x;
     if (before < remaining && remaining <= before + ne) {
       int cnt = before;
       for (int c = my0; c < my1; ++c) {
-        if (key(c) == T && ++cnt == remaining) {
-          sh_i[4] = c;
+        if (key(c) == prefix && ++cnt == remaining) {
+          S.i[4] = c;
           break;
         }
       }
     }
     __syncthreads();
-    c_cut = sh_i[4];
+    c_cut = S.i[4];
   }
-  auto is_sel = [&](uint32_t k, int c) { return any && (k > T || (k == T && c <= c_cut)); };
-
+  auto is_sel = [&](uint32_t k, int c) {
+    return any && k != 0u &&
+           ((k & mask) > prefix || ((k & mask) == prefix && (!tie_cut || c <= c_cut)));
+  };
   // ordered compaction: ids ascending, exclusive prefix of member counts
   int nsel = 0, ntok = 0;
   for (int c = my0; c < my1; ++c) {
     if (is_sel(key(c), c)) {
       ++nsel;
-      ntok += sz[c];
+      ntok += __ldg(sz + c);
     }
   }
   int2 total;
-  const int2 ex = block_scan2(make_int2(nsel, ntok), sh_scan, &total);
+  const int2 ex = block_scan2(make_int2(nsel, ntok), S.scan, &total);
   int* ids = a.sel_ids + (size_t)bh * r;
   int* pre = a.sel_prefix + (size_t)bh * (r + 1);
   int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
@@ -298,29 +320,112 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(DecodeArgs a, in
       pre[pos] = tok;
       if (topk) topk[pos] = c;
       ++pos;
-      tok += sz[c];
+      tok += __ldg(sz + c);
     }
   }
-  for (int i = total.x + tid; i <= r; i += kSelThreads) {
+  for (int i = total.x + tid; i <= r; i += kK2Threads) {
     pre[i] = total.y;
     if (i < r) {
       ids[i] = -1;
       if (topk) topk[i] = -1;
     }
   }
-  uint32_t* mk = a.sel_mask + (size_t)bh * a.n_words;
-  for (int w = tid; w < a.n_words; w += kSelThreads) {
-    uint32_t bits = 0;
-    for (int j = 0; j < 32; ++j) {
-      const int c = 32 * w + j;
-      if (c < C && is_sel(key(c), c)) bits |= 1u << j;
+}
+
+// Role (b): estimate of every non-empty cluster of a 256-cluster chunk of one
+// KV head, for each of its G query heads.  Warp w takes 16 consecutive
+// clusters: lane i < 16 computes e^{s - m_warp} for cluster i (m_warp = the
+// warp's max score), then the 16 value-sum rows are streamed with 128-bit
+// loads and accumulated with the broadcast weights.
+template <int G>
+__device__ void estimate_all(const DecodeArgs& a, int bg, int chunk, float* red) {
+  float(*red_o)[G][kD] = reinterpret_cast<float(*)[G][kD]>(red);
+  float* red_m = red + kK2Warps * G * kD;
+  float* red_l = red_m + kK2Warps * G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int c_end = min(a.C, (chunk + 1) * kEstChunk);
+  const int base = chunk * kEstChunk + warp * kEstBatch;
+  const int c = base + (lane & 15);
+  const bool valid = c < c_end;
+  const int n = valid ? __ldg(a.size + (size_t)bg * a.C + c) : 0;
+  float p[G], mw[G], lw[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const size_t bh = (size_t)b * a.Hq + g * G + h;
+    const float s = (n > 0) ? __ldcg(a.scores + bh * a.C + c) * kLog2e : -INFINITY;
+    float m = s;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    mw[h] = m;
+    p[h] = (s > -INFINITY) ? exp2f(s - m) : 0.f;
+    lw[h] = lane < 16 ? p[h] * (float)n : 0.f;
+  }
+  const float4* vs = reinterpret_cast<const float4*>(a.vsum + ((size_t)bg * a.C) * kD);
+  float4 v[kEstBatch];
+#pragma unroll
+  for (int j = 0; j < kEstBatch; ++j)
+    v[j] = (base + j < c_end) ? __ldg(vs + (size_t)(base + j) * (kD / 4) + lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kEstBatch; ++j) {
+      const float pj = __shfl_sync(kFull, p[h], j);
+      acc0 += pj * v[j].x;
+      acc1 += pj * v[j].y;
+      acc2 += pj * v[j].z;
+      acc3 += pj * v[j].w;
     }
-    mk[w] = bits;
+    lw[h] = warp_sum(lw[h]);
+    reinterpret_cast<float4*>(red_o[warp][h])[lane] = make_float4(acc0, acc1, acc2, acc3);
+    if (lane == 0) {
+      red_m[warp * G + h] = mw[h];
+      red_l[warp * G + h] = lw[h];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kD; idx += kK2Threads) {
+    const int h = idx / kD, dim = idx - h * kD;
+    float M = -INFINITY;
+    for (int w = 0; w < kK2Warps; ++w) M = fmaxf(M, red_m[w * G + h]);
+    float L = 0.f, O = 0.f;
+    if (M > -INFINITY) {
+      for (int w = 0; w < kK2Warps; ++w) {
+        const float mwh = red_m[w * G + h];
+        const float f = mwh > -INFINITY ? exp2f(mwh - M) : 0.f;
+        L += red_l[w * G + h] * f;
+        O += red_o[w][h][dim] * f;
+      }
+    }
+    const size_t bh = (size_t)b * a.Hq + g * G + h;
+    float* P = a.est_part + (bh * a.est_chunks + chunk) * kPartStride;
+    if (dim == 0) {
+      P[0] = (L > 0.f) ? M : -INFINITY;
+      P[1] = L;
+    }
+    P[2 + dim] = O;
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kK2Threads) select_kernel(DecodeArgs a, int n_sel, int cached) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ SelShared S;
+  grid_dep_launch();
+  grid_dep_wait();
+  if ((int)blockIdx.x < n_sel) {
+    select_head(a, blockIdx.x, reinterpret_cast<uint32_t*>(smem), S, cached);
+  } else {
+    const int idx = blockIdx.x - n_sel;
+    const int bg = idx / a.est_chunks;
+    estimate_all<G>(a, bg, idx - bg * a.est_chunks, reinterpret_cast<float*>(smem));
   }
 }
 
 // --------------------------------------------------------------------------
-// K3 + K4: exact attention (steady + retrieved) and estimation, one launch
+// K3: exact attention + retrieved-estimate subtraction + merge
 // --------------------------------------------------------------------------
 constexpr int kAttThreads = 256;
 constexpr int kAttWarps = kAttThreads / 32;
@@ -331,22 +436,51 @@ constexpr int kWinCap = 512;   // retrieved clusters staged per window
 struct __align__(128) AttSmem {
   uint16_t k[kStages][kTile * kD];  // bulk-copy destinations: 16-byte aligned
   uint16_t v[kStages][kTile * kD];
-  float red_o[kAttWarps][kD];       // written as float4: 16-byte aligned
-  float red_m[kAttWarps];
-  float red_l[kAttWarps];
+  float red_o[2][kAttWarps][kD];    // written as float4: 16-byte aligned
+  float red_m[2][kAttWarps];
+  float red_l[2][kAttWarps];
   unsigned long long bar[kStages];  // mbarriers: 8-byte aligned
   int win_prefix[kWinCap + 1];
   int win_row[kWinCap];
+  int win_cid[kWinCap];
+  int last;
 };
 static_assert(offsetof(AttSmem, v) % 128 == 0, "staging buffer alignment");
 static_assert(offsetof(AttSmem, red_o) % 16 == 0, "float4 reduction buffer alignment");
 static_assert(offsetof(AttSmem, bar) % 8 == 0, "mbarrier alignment");
+// the merge reuses the staging buffers (K and V, all stages) for per-partial weights
+constexpr int kMergeMaxPartials = (int)(2 * sizeof(uint16_t) * kStages * kTile * kD / sizeof(float));
 
-template <int G>
-struct EstSmem {
-  float red_o[kAttWarps][G][kD];  // offset 0, written as float4
-  float red_l[kAttWarps][G];
-};
+__device__ void combine_warps(AttSmem& S, int slot, float m_run, float l_run, float o0, float o1,
+                              float o2, float o3, float sign, float* P, bool ok) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) {
+    S.red_m[slot][warp] = m_run;
+    S.red_l[slot][warp] = l_run;
+  }
+  reinterpret_cast<float4*>(S.red_o[slot][warp])[lane] = make_float4(o0, o1, o2, o3);
+  __syncthreads();
+  if (tid < kD) {
+    float M = -INFINITY;
+    for (int w = 0; w < kAttWarps; ++w) M = fmaxf(M, S.red_m[slot][w]);
+    float L = 0.f, O = 0.f;
+    if (ok && M > -INFINITY) {
+      for (int w = 0; w < kAttWarps; ++w) {
+        const float mw = S.red_m[slot][w];
+        const float f = mw > -INFINITY ? exp2f(mw - M) : 0.f;
+        L += S.red_l[slot][w] * f;
+        O += S.red_o[slot][w][tid] * f;
+      }
+    } else {
+      M = -INFINITY;
+    }
+    if (tid == 0) {
+      P[0] = M;
+      P[1] = sign * L;
+    }
+    P[2 + tid] = sign * O;
+  }
+}
 
 __device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -356,6 +490,8 @@ __device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
   const uint16_t* Vh = a.V + head * (size_t)a.N * kD;
   const uint16_t* Ksh = a.ksorted + head * (size_t)a.N_idx * kD;
   const uint16_t* Vsh = a.vsorted + head * (size_t)a.N_idx * kD;
+  const float4* vsum = reinterpret_cast<const float4*>(a.vsum + head * (size_t)a.C * kD);
+  const float* sc = a.scores + (size_t)bh * a.C;
   const int* off = a.offset + head * (size_t)(a.C + 1);
   const int* ids = a.sel_ids + (size_t)bh * a.r;
   const int* pre = a.sel_prefix + (size_t)bh * (a.r + 1);
@@ -376,11 +512,14 @@ __device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
   __syncthreads();
 
   float m_run = -INFINITY, l_run = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  // estimates of the retrieved clusters whose first token lies in this block
+  float m_neg = -INFINITY, l_neg = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
   uint32_t phase = 0;
   bool ok = true;
   int round_lo = lo;
   while (ok && round_lo < hi) {
     int round_hi = hi;
+    int n_cl = 0;
     if (hi > ns) {
       // window of retrieved clusters overlapping [round_lo, hi)
       const int lo_u = max(round_lo - ns, 0), hi_u = hi - ns;
@@ -392,13 +531,17 @@ __device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
         cnt_lt += __syncthreads_count(p < hi_u);
       }
       const int i0 = cnt_le - 1;
-      int n_cl = cnt_lt - i0;
+      n_cl = cnt_lt - i0;
       if (n_cl > kWinCap) {
         n_cl = kWinCap;
         round_hi = ns + pre[i0 + kWinCap];
       }
       for (int j = tid; j <= n_cl; j += kAttThreads) S.win_prefix[j] = pre[i0 + j];
-      for (int j = tid; j < n_cl; j += kAttThreads) S.win_row[j] = off[ids[i0 + j]];
+      for (int j = tid; j < n_cl; j += kAttThreads) {
+        const int c = ids[i0 + j];
+        S.win_cid[j] = c;
+        S.win_row[j] = off[c];
+      }
       __syncthreads();
     }
     const int ntiles = (round_hi - round_lo + kTile - 1) / kTile;
@@ -452,6 +595,27 @@ __device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
     if (tid == 0)
       for (int t = 0; t < min(kStages, ntiles); ++t)
         if (!(skip_first && t == 0)) issue(t, t);
+
+    // while the first copies are in flight: the estimates to subtract, one
+    // warp per cluster (clusters that start inside this round)
+    for (int j = warp; j < n_cl; j += kAttWarps) {
+      const int start = ns + S.win_prefix[j];
+      if (start < round_lo || start >= round_hi) continue;
+      const int c = S.win_cid[j];
+      const float s = __ldcg(sc + c) * kLog2e;
+      const float n = (float)(S.win_prefix[j + 1] - S.win_prefix[j]);
+      const float4 vv = __ldg(vsum + (size_t)c * (kD / 4) + lane);
+      const float m_new = fmaxf(m_neg, s);
+      const float corr = exp2f(m_neg - m_new);
+      const float p = exp2f(s - m_new);
+      l_neg = l_neg * corr + p * n;
+      n0 = n0 * corr + p * vv.x;
+      n1 = n1 * corr + p * vv.y;
+      n2 = n2 * corr + p * vv.z;
+      n3 = n3 * corr + p * vv.w;
+      m_neg = m_new;
+    }
+
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % kStages;
       const int ntok = min(kTile, round_hi - (round_lo + t * kTile));
@@ -517,172 +681,82 @@ __device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
     round_lo = round_hi;
     __syncthreads();
   }
-  // combine the warps
-  if (lane == 0) {
-    S.red_m[warp] = m_run;
-    S.red_l[warp] = l_run;
-  }
-  reinterpret_cast<float4*>(S.red_o[warp])[lane] = make_float4(o0, o1, o2, o3);
-  __syncthreads();
-  if (tid < kD) {
-    float M = -INFINITY;
-    for (int w = 0; w < kAttWarps; ++w) M = fmaxf(M, S.red_m[w]);
-    float L = 0.f, O = 0.f;
-    if (ok && M > -INFINITY) {
-      for (int w = 0; w < kAttWarps; ++w) {
-        const float f = exp2f(S.red_m[w] - M);
-        L += S.red_l[w] * f;
-        O += S.red_o[w][tid] * f;
-      }
-    } else {
-      M = -INFINITY;
-    }
-    float* P = a.att_part + ((size_t)bh * a.att_splits + sp) * kPartStride;
-    if (tid == 0) {
-      P[0] = M;
-      P[1] = L;
-    }
-    P[2 + tid] = O;
-  }
+  float* P = a.att_part + ((size_t)bh * a.att_splits + sp) * 2 * kPartStride;
+  combine_warps(S, 0, m_run, l_run, o0, o1, o2, o3, 1.f, P, ok);
+  combine_warps(S, 1, m_neg, l_neg, n0, n1, n2, n3, -1.f, P + kPartStride, ok);
 }
 
-template <int G>
-__device__ void estimate_clusters(const DecodeArgs& a, int bg, int chunk, EstSmem<G>& S) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-  const int c_begin = chunk * a.est_chunk_clusters;
-  const int c_end = min(a.C, c_begin + a.est_chunk_clusters);
-  const float4* vs = reinterpret_cast<const float4*>(a.vsum + (size_t)bg * a.C * kD);
-  const int* sz = a.size + (size_t)bg * a.C;
-  float hm[G];
-  const float* sc[G];
-  const uint32_t* mk[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const size_t bh = (size_t)b * a.Hq + g * G + h;
-    hm[h] = a.head_max[bh] * kLog2e;
-    sc[h] = a.scores + bh * a.C;
-    mk[h] = a.sel_mask + bh * a.n_words;
-  }
-  float acc[G][4];
-  float lsum[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    lsum[h] = 0.f;
-    acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
-  }
-  for (int base = c_begin + warp * 32; base < c_end; base += kAttWarps * 32) {
-    const int c = base + lane;
-    const bool valid = c < c_end;
-    const int n = valid ? __ldg(sz + c) : 0;
-    float p[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const bool sel = valid && ((__ldg(mk[h] + (c >> 5)) >> (c & 31)) & 1u);
-      p[h] = (n > 0 && !sel) ? exp2f(__ldg(sc[h] + c) * kLog2e - hm[h]) : 0.f;
-      lsum[h] += p[h] * (float)n;
-    }
-    const int cnt = min(32, c_end - base);
-#pragma unroll 1
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u;
-        v[u] = (j < cnt) ? __ldg(vs + (size_t)(base + j) * (kD / 4) + lane)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pj = __shfl_sync(kFull, p[h], j0 + u);
-          acc[h][0] += pj * v[u].x;
-          acc[h][1] += pj * v[u].y;
-          acc[h][2] += pj * v[u].z;
-          acc[h][3] += pj * v[u].w;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    lsum[h] = warp_sum(lsum[h]);
-    reinterpret_cast<float4*>(S.red_o[warp][h])[lane] =
-        make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-    if (lane == 0) S.red_l[warp][h] = lsum[h];
-  }
-  __syncthreads();
-  for (int idx = tid; idx < G * kD; idx += kAttThreads) {
-    const int h = idx / kD, dim = idx - h * kD;
-    float O = 0.f, L = 0.f;
-    for (int w = 0; w < kAttWarps; ++w) {
-      O += S.red_o[w][h][dim];
-      L += S.red_l[w][h];
-    }
-    const size_t bh = (size_t)b * a.Hq + g * G + h;
-    float* P = a.est_part + (bh * a.est_chunks + chunk) * kPartStride;
-    if (dim == 0) {
-      P[0] = (L > 0.f) ? a.head_max[bh] * kLog2e : -INFINITY;
-      P[1] = L;
-    }
-    P[2 + dim] = O;
-  }
-}
-
-template <int G>
-__global__ void __launch_bounds__(kAttThreads) attend_kernel(DecodeArgs a, int n_att_blocks) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  grid_dep_launch();
-  grid_dep_wait();
-  if ((int)blockIdx.x < n_att_blocks) {
-    const int bh = blockIdx.x / a.att_splits;
-    const int sp = blockIdx.x - bh * a.att_splits;
-    attend_tokens(a, bh, sp, *reinterpret_cast<AttSmem*>(smem));
-  } else {
-    const int idx = blockIdx.x - n_att_blocks;
-    const int bg = idx / a.est_chunks;
-    const int chunk = idx - bg * a.est_chunks;
-    estimate_clusters<G>(a, bg, chunk, *reinterpret_cast<EstSmem<G>*>(smem));
-  }
-}
-
-// --------------------------------------------------------------------------
-// K5: log-sum-exp merge
-// --------------------------------------------------------------------------
-__global__ void __launch_bounds__(kD) merge_kernel(DecodeArgs a) {
-  __shared__ float sh_m[kD / 32];
-  grid_dep_launch();
-  grid_dep_wait();
-  const int bh = blockIdx.x, tid = threadIdx.x;
-  const float* PA = a.att_part + (size_t)bh * a.att_splits * kPartStride;
+// Log-sum-exp merge of every partial of one query head: exact (+), retrieved
+// estimates (-) and estimation chunks (+).
+__device__ void merge_head(const DecodeArgs& a, int bh, AttSmem& S) {
+  const int tid = threadIdx.x;
+  float* w = reinterpret_cast<float*>(S.k);  // per-partial weight (reuses staging)
+  __shared__ float sh_red[kAttWarps];
+  const int n_att = 2 * a.att_splits;
+  const int P = n_att + a.est_chunks;
+  const float* PA = a.att_part + (size_t)bh * n_att * kPartStride;
   const float* PE = a.est_part + (size_t)bh * a.est_chunks * kPartStride;
-  const int P = a.att_splits + a.est_chunks;
   auto part = [&](int i) {
-    return i < a.att_splits ? PA + (size_t)i * kPartStride
-                            : PE + (size_t)(i - a.att_splits) * kPartStride;
+    return i < n_att ? PA + (size_t)i * kPartStride : PE + (size_t)(i - n_att) * kPartStride;
   };
   float M = -INFINITY;
-  for (int i = tid; i < P; i += kD) M = fmaxf(M, part(i)[0]);
-  M = warp_max(M);
-  if ((tid & 31) == 0) sh_m[tid >> 5] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(sh_m[0], sh_m[1]), fmaxf(sh_m[2], sh_m[3]));
-  float L = 0.f, O = 0.f;
-  if (M > -INFINITY) {
-#pragma unroll 4
-    for (int i = 0; i < P; ++i) {
-      const float* p = part(i);
-      const float m = p[0];
-      if (m > -INFINITY) {
-        const float f = exp2f(m - M);
-        L += p[1] * f;
-        O += p[2 + tid] * f;
-      }
-    }
+  for (int i = tid; i < P; i += kAttThreads) {
+    const float m = __ldcg(part(i));
+    w[i] = m;
+    M = fmaxf(M, m);
   }
-  a.out[(size_t)bh * kD + tid] = (L > 0.f) ? O / L : 0.f;
-  if (a.lse != nullptr && tid == 0) a.lse[bh] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+  M = warp_max(M);
+  if ((tid & 31) == 0) sh_red[tid >> 5] = M;
+  __syncthreads();
+  M = -INFINITY;
+  for (int i = 0; i < kAttWarps; ++i) M = fmaxf(M, sh_red[i]);
+  __syncthreads();
+  float L = 0.f;
+  for (int i = tid; i < P; i += kAttThreads) {
+    const float m = w[i];
+    const float f = (M > -INFINITY && m > -INFINITY) ? exp2f(m - M) : 0.f;
+    w[i] = f;
+    L += f * __ldcg(part(i) + 1);
+  }
+  L = warp_sum(L);
+  if ((tid & 31) == 0) sh_red[tid >> 5] = L;
+  __syncthreads();
+  L = 0.f;
+  for (int i = 0; i < kAttWarps; ++i) L += sh_red[i];
+  // two threads per output dimension, each over half of the partials
+  const int dim = tid & (kD - 1), half = tid >> 7;
+  float O = 0.f;
+#pragma unroll 4
+  for (int i = half; i < P; i += 2) O += w[i] * __ldcg(part(i) + 2 + dim);
+  float* red = reinterpret_cast<float*>(S.red_o);
+  __syncthreads();
+  if (half == 1) red[dim] = O;
+  __syncthreads();
+  if (half == 0) {
+    O += red[dim];
+    a.out[(size_t)bh * kD + dim] = (L > 0.f) ? O / L : 0.f;
+    if (a.lse != nullptr && dim == 0) a.lse[bh] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+}
+
+__global__ void __launch_bounds__(kAttThreads) attend_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  AttSmem& S = *reinterpret_cast<AttSmem*>(smem);
+  grid_dep_launch();
+  grid_dep_wait();
+  const int bh = blockIdx.x / a.att_splits;
+  const int sp = blockIdx.x - bh * a.att_splits;
+  attend_tokens(a, bh, sp, S);
+  // the last block of this head to finish merges all of its partials
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) S.last = (atomicAdd(&a.counters[bh], 1) == a.att_splits - 1);
+  __syncthreads();
+  if (S.last) {
+    __threadfence();
+    merge_head(a, bh, S);
+    if (threadIdx.x == 0) a.counters[bh] = 0;  // ready for the next call
+  }
 }
 
 template <typename F>
@@ -696,8 +770,9 @@ cudaError_t set_smem(F* f, size_t bytes) {
 // launchers
 // --------------------------------------------------------------------------
 cudaError_t launch_decode_score(const DecodeArgs& a, cudaStream_t st) {
-  const int rows_per_sweep = (kScoreThreads / 32) * (32 / a.G);
-  const long long target_blocks = 148LL * 8;
+  const int rows = 32 / a.G;
+  const int rows_per_sweep = kScoreWarps * (rows >= 16 ? rows : 2 * rows);
+  const long long target_blocks = 148LL * 4;
   const long long rows_total = (long long)a.C * a.B * a.Hkv;
   long long rpb = (rows_total + target_blocks - 1) / target_blocks;
   rpb = ((rpb + rows_per_sweep - 1) / rows_per_sweep) * rows_per_sweep;
@@ -713,46 +788,47 @@ cudaError_t launch_decode_score(const DecodeArgs& a, cudaStream_t st) {
   }
 }
 
-cudaError_t launch_decode_select(const DecodeArgs& a, cudaStream_t st) {
-  const int cached = a.C <= kSelCacheMax ? 1 : 0;
-  const size_t smem = cached ? (size_t)a.C * sizeof(uint32_t) : 0;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = set_smem(select_kernel, (size_t)kSelCacheMax * sizeof(uint32_t));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return launch_ex(select_kernel, dim3((unsigned)(a.B * a.Hq)), dim3(kSelThreads), smem, st, true,
-                   a, cached);
-}
-
 template <int G>
-static cudaError_t launch_attend_g(const DecodeArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(AttSmem) > sizeof(EstSmem<G>) ? sizeof(AttSmem) : sizeof(EstSmem<G>);
+static cudaError_t launch_select_g(const DecodeArgs& a, cudaStream_t st) {
+  const int cached = a.C <= kSelCacheMax ? 1 : 0;
+  const size_t sel_smem = cached ? (size_t)a.C * sizeof(uint32_t) : 0;
+  const size_t est_smem = sizeof(float) * (size_t)kK2Warps * G * (kD + 2);
+  const size_t smem = sel_smem > est_smem ? sel_smem : est_smem;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = set_smem(attend_kernel<G>, smem);
+    const size_t mx = (size_t)kSelCacheMax * sizeof(uint32_t) > est_smem
+                          ? (size_t)kSelCacheMax * sizeof(uint32_t)
+                          : est_smem;
+    cudaError_t e = set_smem(select_kernel<G>, mx);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int n_att = a.B * a.Hq * a.att_splits;
+  const int n_sel = a.B * a.Hq;
   const int n_est = a.B * a.Hkv * a.est_chunks;
-  return launch_ex(attend_kernel<G>, dim3((unsigned)(n_att + n_est)), dim3(kAttThreads), smem, st,
-                   true, a, n_att);
+  return launch_ex(select_kernel<G>, dim3((unsigned)(n_sel + n_est)), dim3(kK2Threads), smem, st,
+                   true, a, n_sel, cached);
 }
 
-cudaError_t launch_decode_attend(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_select(const DecodeArgs& a, cudaStream_t st) {
   switch (a.G) {
-    case 1: return launch_attend_g<1>(a, st);
-    case 2: return launch_attend_g<2>(a, st);
-    case 4: return launch_attend_g<4>(a, st);
-    case 8: return launch_attend_g<8>(a, st);
+    case 1: return launch_select_g<1>(a, st);
+    case 2: return launch_select_g<2>(a, st);
+    case 4: return launch_select_g<4>(a, st);
+    case 8: return launch_select_g<8>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st) {
-  return launch_ex(merge_kernel, dim3((unsigned)(a.B * a.Hq)), dim3(kD), 0, st, true, a);
+cudaError_t launch_decode_attend(const DecodeArgs& a, cudaStream_t st) {
+  if (a.est_chunks + 2 * a.att_splits > kMergeMaxPartials) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = set_smem(attend_kernel, sizeof(AttSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(attend_kernel, dim3((unsigned)(a.B * a.Hq * a.att_splits)), dim3(kAttThreads),
+                   sizeof(AttSmem), st, true, a);
 }
 
 }  // namespace wi

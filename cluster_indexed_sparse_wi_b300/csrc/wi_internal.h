@@ -39,7 +39,7 @@ struct BuildArgs {
 };
 
 struct DecodeArgs {
-  int B, Hq, Hkv, G, N, sink, window, r, C, N_idx, n_words;
+  int B, Hq, Hkv, G, N, sink, window, r, C, N_idx;
   float scale;
   const uint16_t* q;        // bf16 [B,Hq,128]
   const uint16_t* K;        // bf16 [B,Hkv,N,128]
@@ -56,8 +56,8 @@ struct DecodeArgs {
   float* head_max;      // [B,Hq]
   int* sel_ids;         // [B,Hq,r]   (r >= 1 slots)
   int* sel_prefix;      // [B,Hq,r+1]
-  uint32_t* sel_mask;   // [B,Hq,n_words]
-  float* att_part;      // [B,Hq,att_splits,2+128]
+  int* counters;        // [B,Hq]  arrival counters of the attention blocks
+  float* att_part;      // [B,Hq,att_splits,2,2+128]  (exact; minus retrieved estimate)
   float* est_part;      // [B,Hq,est_chunks,2+128]
   int att_splits, est_chunks, est_chunk_clusters;
   int inject;           // test hook: block 0 skips its first staging copy
@@ -73,7 +73,7 @@ constexpr int kPartStride = 2 + 128;  // (m, l, o[128]) per partial
 cudaError_t launch_decode_score(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_select(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_attend(const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st);
+constexpr int kEstChunk = 256;  // clusters per estimation block
 
 // build launchers (wi_build.cu)
 cudaError_t launch_build_init(const BuildArgs& a, cudaStream_t st);

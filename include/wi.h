@@ -187,13 +187,14 @@ WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_cluster
 /* Byte offsets of the decode workspace regions (host struct), for
  * inspection of intermediate results.  No device work. */
 typedef struct {
-  size_t scores;        /* f32 [B,Hq,C]    s_c = scale q.kbar_c, -inf if empty   */
-  size_t head_max;      /* f32 [B,Hq]      max_c s_c                            */
-  size_t selected;      /* i32 [B,Hq,r]    retrieved ids ascending, -1 padding   */
-  size_t sel_prefix;    /* i32 [B,Hq,r+1]  exclusive prefix of selected sizes    */
-  size_t sel_mask;      /* u32 [B,Hq,ceil(C/32)] bit c set = c retrieved          */
-  size_t att_partials;  /* f32 [B,Hq,att_splits,2+d]  (m, l, o) in log2 units     */
-  size_t est_partials;  /* f32 [B,Hq,est_chunks,2+d]                             */
+  size_t scores;        /* f32 [B,Hq,C]    s_c = scale q.kbar_c, -inf if empty    */
+  size_t head_max;      /* f32 [B,Hq]      max_c s_c                             */
+  size_t selected;      /* i32 [B,Hq,r]    retrieved ids ascending, -1 padding    */
+  size_t sel_prefix;    /* i32 [B,Hq,r+1]  exclusive prefix of selected sizes     */
+  size_t counters;      /* i32 [B,Hq]      arrival counters (zero between calls)  */
+  size_t att_partials;  /* f32 [B,Hq,att_splits,2,2+d]  (m, l, o), log2 units:
+                           exact part, then minus the retrieved clusters' estimate */
+  size_t est_partials;  /* f32 [B,Hq,est_chunks,2+d]  estimate of every cluster   */
   size_t total;
   int att_splits, est_chunks, est_chunk_clusters, reserved;
 } wi_decode_layout;
@@ -211,34 +212,34 @@ WI_API int wi_decode_workspace_layout(const wi_decode_params *p, int n_clusters,
  *   L    = sum_S e^{l_i - M} + sum_E n_c e^{s_c - M},
  *   out  = (sum_S e^{l_i - M} v_i + sum_E e^{s_c - M} value_sum_c) / L,
  *   lse  = M + ln L  (log-sum-exp merge of the three zones).
+ * The E sums are formed as (all non-empty clusters) minus (clusters in T), in
+ * f32; this reorders the arithmetic only.
  * q: bf16 [B,Hq,d]; out: f32 [B,Hq,d]; lse: f32 [B,Hq] or NULL;
  * topk_ids: i32 [B,Hq,r] (ascending ids, -1 padding) or NULL.
- * Equivalent to wi_decode_score, wi_decode_select, wi_decode_attend,
- * wi_decode_merge in that order. */
+ * Equivalent to wi_decode_score, wi_decode_select, wi_decode_attend in order. */
 WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const void *K, const void *V,
                         const wi_index *index, float *out, float *lse, int32_t *topk_ids,
                         void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 1: cluster scores s into the workspace (centroid scan). */
+/* Decode stage 1: cluster scores s into the workspace (centroid-key scan). */
 WI_API int wi_decode_score(const wi_decode_params *p, const void *q, const wi_index *index,
                     void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 2: per query head, the retrieval set T (radix select over the
- * scores; ties to the lower id), its size prefix and bit mask, and the head's
- * maximum score.  topk_ids may be NULL. */
+/* Decode stage 2, one launch with two roles: per query head, the retrieval
+ * set T (radix select over the scores; ties to the lower id) with its token
+ * prefix and the head's maximum score; and, per chunk of clusters, the
+ * estimate of every non-empty cluster (log2-unit partials).  topk_ids may be
+ * NULL. */
 WI_API int wi_decode_select(const wi_decode_params *p, const wi_index *index, int32_t *topk_ids,
                      void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 3: exact attention partials over the steady zone and the
- * retrieved clusters (split over the token list), and estimation partials
- * over the other non-empty clusters (split over cluster chunks). */
+/* Decode stage 3: exact attention over the steady zone and the retrieved
+ * clusters (split over each head's token list), the retrieved clusters'
+ * estimates with a negative sign, and the log-sum-exp merge of all partials
+ * into out and lse (lse may be NULL). */
 WI_API int wi_decode_attend(const wi_decode_params *p, const void *q, const void *K, const void *V,
-                     const wi_index *index, void *workspace, size_t workspace_bytes,
-                     wi_stream_t stream);
-
-/* Decode stage 4: log-sum-exp merge of all partials into out and lse. */
-WI_API int wi_decode_merge(const wi_decode_params *p, const wi_index *index, float *out, float *lse,
-                    void *workspace, size_t workspace_bytes, wi_stream_t stream);
+                     const wi_index *index, float *out, float *lse, void *workspace,
+                     size_t workspace_bytes, wi_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the device status word at the
  * start of `workspace` into *device_status (host).  Returns WI_OK, or

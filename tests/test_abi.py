@@ -119,7 +119,7 @@ def test_decode_layout(L):
     lay = L.DecodeLayout()
     assert lib.wi_decode_workspace_layout(ctypes.byref(dp(L)), 256, ctypes.byref(lay)) == 0
     assert lay.total == lib.wi_decode_workspace_bytes(ctypes.byref(dp(L)), 256)
-    regions = [lay.scores, lay.head_max, lay.selected, lay.sel_prefix, lay.sel_mask,
+    regions = [lay.scores, lay.head_max, lay.selected, lay.sel_prefix, lay.counters,
                lay.att_partials, lay.est_partials, lay.total]
     assert regions == sorted(regions) and all(r % 256 == 0 for r in regions)
     assert lay.head_max - lay.scores >= 8 * 256 * 4

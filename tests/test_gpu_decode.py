@@ -219,7 +219,6 @@ def test_repeated_calls_are_deterministic_and_status_clean():
     dec.score(q)
     dec.select(with_topk=True)
     dec.attend(q, K, V)
-    dec.merge()
     torch.cuda.synchronize()
     assert torch.equal(dec.out, o1)
 
