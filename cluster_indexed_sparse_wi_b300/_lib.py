@@ -23,6 +23,7 @@ WI_HEAD_DIM = 128
 WI_MAX_K_PER_SEG = 512
 WI_MAX_SEG_LEN = 16384
 WI_MAX_CLUSTERS = 1 << 20
+WI_STATIC_SCRATCH_BYTES = 16 << 20
 
 FIELDS = ["centroid_key", "unit_centroid", "value_sum", "size", "offset", "perm", "assign",
           "k_sorted", "v_sorted"]
@@ -32,7 +33,7 @@ SYMBOLS = [
     "wi_index_sizes", "wi_build_workspace_bytes", "wi_build_index", "wi_build_init",
     "wi_kmeans_assign", "wi_kmeans_update", "wi_build_finalize", "wi_decode_workspace_bytes",
     "wi_decode_workspace_layout", "wi_decode_attention", "wi_decode_score", "wi_decode_select",
-    "wi_decode_attend", "wi_sync_status", "wi_status_string", "wi_debug_inject",
+    "wi_decode_attend", "wi_decode_attention_static", "wi_sync_status", "wi_status_string", "wi_debug_inject",
     "wi_version",
 ]
 
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
         "wi_decode_score": (i, [dp, vp, ip, vp, sz, vp]),
         "wi_decode_select": (i, [dp, ip, vp, vp, sz, vp]),
         "wi_decode_attend": (i, [dp, vp, vp, vp, ip, vp, vp, vp, sz, vp]),
+        "wi_decode_attention_static": (i, [dp, vp, vp, vp, ip, vp, vp, vp, vp]),
         "wi_sync_status": (i, [vp, vp, P(i)]),
         "wi_status_string": (ctypes.c_char_p, [i]),
         "wi_debug_inject": (i, [i]),

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libwi.so")
-SOURCES = ["wi_api.cu", "wi_decode.cu", "wi_build.cu", "wi_assign.cu"]
+SOURCES = ["wi_api.cu", "wi_decode.cu", "wi_build.cu", "wi_assign.cu", "wi_static.cu"]
 HEADERS = ["wi_device.cuh", "wi_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

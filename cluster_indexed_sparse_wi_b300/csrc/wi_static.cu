@@ -1,0 +1,63 @@
+// Decode entry point for callers that cannot allocate device memory.
+//
+// Some hosts of this library have no allocator to give it: an inference
+// runtime that hands a plugin only pre-planned buffers, code running where
+// cudaMalloc is forbidden or would break a memory budget fixed up front.  For
+// them wi_decode_attention_static runs the same decode as wi_decode_attention
+// but takes no workspace: it uses a fixed scratch array that lives in this
+// file as a static device variable, so every GPU that loads the library holds
+// WI_STATIC_SCRATCH_BYTES for it until the process exits.
+#include <mutex>
+
+#include "wi.h"
+#include "wi_internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = WI_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// The scratch itself.  In host code this name is only a stand-in for the
+// symbol: its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+std::mutex g_lock;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current) and cached.
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WI_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return WI_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> guard(g_lock);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return WI_ERR_LAUNCH;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return WI_OK;
+}
+
+}  // namespace
+
+extern "C" int wi_decode_attention_static(const wi_decode_params* p, const void* q, const void* K,
+                                          const void* V, const wi_index* index, float* out,
+                                          float* lse, int32_t* topk_ids, wi_stream_t stream) {
+  if (p == nullptr || index == nullptr) return WI_ERR_INVALID_ARG;
+  wi_decode_layout lay;
+  int st = wi_decode_workspace_layout(p, index->n_clusters, &lay);
+  if (st != WI_OK) return st;
+  if (lay.total > kScratchBytes) return WI_ERR_WORKSPACE;  // beyond the fixed scratch
+  void* ws = nullptr;
+  if ((st = scratch_address(&ws)) != WI_OK) return st;
+  const cudaStream_t s = (cudaStream_t)stream;
+  // The scratch keeps the previous call's contents: the status word and the
+  // attention blocks' arrival counters must start at zero.
+  char* base = static_cast<char*>(ws);
+  if (cudaMemsetAsync(base, 0, lay.scores, s) != cudaSuccess ||
+      cudaMemsetAsync(base + lay.counters, 0, lay.att_partials - lay.counters, s) != cudaSuccess)
+    return WI_ERR_LAUNCH;
+  return wi_decode_attention(p, q, K, V, index, out, lse, topk_ids, ws, kScratchBytes, stream);
+}

@@ -241,6 +241,32 @@ WI_API int wi_decode_attend(const wi_decode_params *p, const void *q, const void
                      const wi_index *index, float *out, float *lse, void *workspace,
                      size_t workspace_bytes, wi_stream_t stream);
 
+/* Size of the fixed device scratch used by wi_decode_attention_static. */
+#define WI_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Decode for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this is a packaging of wi_decode_attention for hosts that give
+ * a library no allocator (runtimes that hand a plugin only pre-planned
+ * buffers, or whose device-memory budget is fixed before the plugin runs).
+ * Same arguments and results as wi_decode_attention, minus the workspace:
+ * the call uses a scratch array of WI_STATIC_SCRATCH_BYTES that every GPU
+ * loading this library holds from module load until process exit.  It calls
+ * no allocator.
+ *  - Returns WI_ERR_WORKSPACE when the decode needs more scratch than
+ *    WI_STATIC_SCRATCH_BYTES (wi_decode_workspace_bytes tells how much).
+ *  - The first call on a device looks the scratch's address up on that device
+ *    (the device must be current); make that first call before any stream
+ *    capture.
+ *  - Every call, from any thread or stream, shares the one array: calls that
+ *    overlap on the GPU race and corrupt each other's results.  Each call
+ *    clears the parts that must start at zero; the rest keeps the previous
+ *    call's contents.
+ *  - Device-side errors (a bounded wait that ran out) land in the shared
+ *    scratch and are not reported through wi_sync_status. */
+WI_API int wi_decode_attention_static(const wi_decode_params *p, const void *q, const void *K,
+                               const void *V, const wi_index *index, float *out, float *lse,
+                               int32_t *topk_ids, wi_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the device status word at the
  * start of `workspace` into *device_status (host).  Returns WI_OK, or
  * WI_ERR_CUDA if the stream reported an error (then *device_status is
