@@ -65,9 +65,9 @@ class IndexStruct(ctypes.Structure):
 
 class DecodeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("scores", "head_max", "selected", "sel_prefix", "counters", "att_partials",
-                 "est_partials", "total")] + [
-        (n, ctypes.c_int) for n in ("att_splits", "est_chunks", "est_chunk_clusters", "reserved")]
+                ("counters", "scores", "head_max", "selected", "sel_rows", "sel_counts",
+                 "partials", "total")] + [
+        (n, ctypes.c_int) for n in ("counter_bytes", "max_blocks", "reserved0", "reserved1")]
 
 
 _lib = None

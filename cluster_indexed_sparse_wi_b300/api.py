@@ -270,13 +270,17 @@ class Decoder:
         c = self.index.cfg
         return self._view(self.layout.head_max, c.B * self.Hq, torch.float32, (c.B, self.Hq))
 
-    def selected(self) -> Tuple[torch.Tensor, torch.Tensor]:
+    def selected(self) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+        """Retrieved ids (ascending, -1 padding), their first sorted rows and
+        their sizes, each [B, Hq, r]."""
         c = self.index.cfg
         rs = max(self.r, 1)
-        ids = self._view(self.layout.selected, c.B * self.Hq * rs, torch.int32, (c.B, self.Hq, rs))
-        pre = self._view(self.layout.sel_prefix, c.B * self.Hq * (self.r + 1), torch.int32,
-                         (c.B, self.Hq, self.r + 1))
-        return ids[..., :self.r], pre
+        shape = (c.B, self.Hq, rs)
+        n = c.B * self.Hq * rs
+        ids = self._view(self.layout.selected, n, torch.int32, shape)
+        rows = self._view(self.layout.sel_rows, n, torch.int32, shape)
+        cnts = self._view(self.layout.sel_counts, n, torch.int32, shape)
+        return ids[..., :self.r], rows[..., :self.r], cnts[..., :self.r]
 
     def status(self, stream=None) -> int:
         return sync_status(self.workspace, stream)
@@ -299,7 +303,7 @@ def capture_graph(fn, device) -> "torch.cuda.CUDAGraph":
 
 class DecodeStep:
     """One decode step as a CUDA graph over host buffers: q is copied from
-    pinned host memory, the four decode kernels run, and out / lse are copied
+    pinned host memory, the decode kernel runs, and out / lse are copied
     back into pinned host memory.  `step(q_host)` replays the graph and waits
     for the results."""
 

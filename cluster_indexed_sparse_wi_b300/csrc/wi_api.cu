@@ -14,7 +14,8 @@ using wi::DecodeArgs;
 
 namespace {
 
-constexpr size_t kStatusBytes = 256;  // status word + reserved counters
+constexpr size_t kStatusBytes = 256;  // status word + reserved
+constexpr size_t kSyncBytes = 256;    // grid-barrier words at the start of the counters region
 std::atomic<int> g_inject{0};         // wi_debug_inject request
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -163,37 +164,37 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   const int st = check_decode(p, C);
   if (st != WI_OK) return st;
   memset(L, 0, sizeof(*L));
-  const long long heads = (long long)p->B * p->Hq;
-  const long long n_idx = (long long)p->N - p->sink - p->window;
-  // expected exact tokens per query head: steady zone + r average clusters
-  const long long est_tokens = p->sink + p->window + ((long long)p->r * n_idx + C - 1) / C;
-  long long splits = (est_tokens + 191) / 192;
-  const long long min_splits = (2 * 148 + heads - 1) / heads;
-  if (splits < min_splits) splits = min_splits;
-  if (splits > 128) splits = 128;
-  if (splits < 1) splits = 1;
-  L->att_splits = (int)splits;
-  L->est_chunk_clusters = wi::kEstChunk;
-  L->est_chunks = (C + L->est_chunk_clusters - 1) / L->est_chunk_clusters;
-  const int r_slots = p->r > 0 ? p->r : 1;
+  const size_t heads = (size_t)p->B * p->Hq;
+  const size_t groups = (size_t)p->B * p->Hkv;
+  const size_t G = (size_t)(p->Hq / p->Hkv);
+  const size_t rs = p->r > 0 ? (size_t)p->r : 1;
+  const size_t part = (size_t)wi::kPartStride * 4;
   size_t off = kStatusBytes;
-  L->scores = off;
-  off += align256((size_t)heads * C * 4);
-  L->head_max = off;
-  off += align256((size_t)heads * 4);
-  L->selected = off;
-  off += align256((size_t)heads * r_slots * 4);
-  L->sel_prefix = off;
-  off += align256((size_t)heads * (p->r + 1) * 4);
   L->counters = off;
-  off += align256((size_t)heads * 4);
-  L->att_partials = off;
-  off += align256((size_t)heads * L->att_splits * 2 * wi::kPartStride * 4);
-  L->est_partials = off;
-  off += align256((size_t)heads * L->est_chunks * wi::kPartStride * 4);
+  L->counter_bytes = (int)align256(kSyncBytes + (2 * groups + 3 * heads) * 4);
+  off += (size_t)L->counter_bytes;
+  L->scores = off;
+  off += align256(heads * (size_t)C * 4);
+  L->head_max = off;
+  off += align256(heads * 4);
+  L->selected = off;
+  off += align256(heads * rs * 4);
+  L->sel_rows = off;
+  off += align256(heads * rs * 4);
+  L->sel_counts = off;
+  off += align256(heads * rs * 4);
+  L->partials = off;
+  off += align256((wi::kMaxBlocks + groups) * G * part);  // estimate of every cluster
+  off += align256((wi::kMaxBlocks + heads) * part);       // steady pieces
+  off += align256((wi::kMaxBlocks + heads) * part);       // retrieved pieces
+  off += align256(heads * part);                          // selected clusters' estimate
   L->total = off;
+  L->max_blocks = wi::kMaxBlocks;
   return WI_OK;
 }
+
+// Cost of one per-head selection in units of one centroid-key tile (64 rows).
+double selection_weight(int C) { return 8.0 + C / 1024.0; }
 
 int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, const void* V,
                      const wi_index* ix, void* ws, size_t ws_bytes, DecodeArgs* a,
@@ -218,6 +219,13 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
     if (q == nullptr || K == nullptr || V == nullptr) return WI_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16)) return WI_ERR_ALIGNMENT;
   }
+  const int C = ix->n_clusters;
+  const int tpg = (C + wi::kDecodeTile - 1) / wi::kDecodeTile;
+  const long long n_tiles = (long long)p->B * p->Hkv * tpg;
+  if (n_tiles >= (1LL << 31)) return WI_ERR_UNSUPPORTED;
+  if ((st = device_ok()) != WI_OK) return st;
+  int nb = 0;
+  if (wi::decode_blocks(&nb) != cudaSuccess || nb < 2) return WI_ERR_LAUNCH;
   memset(a, 0, sizeof(*a));
   char* w = static_cast<char*>(ws);
   a->B = p->B;
@@ -228,7 +236,7 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->sink = p->sink;
   a->window = p->window;
   a->r = p->r;
-  a->C = ix->n_clusters;
+  a->C = C;
   a->N_idx = p->N - p->sink - p->window;
   a->scale = p->scale;
   a->q = static_cast<const uint16_t*>(q);
@@ -241,17 +249,74 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->ksorted = static_cast<const uint16_t*>(ix->k_sorted);
   a->vsorted = static_cast<const uint16_t*>(ix->v_sorted);
   a->status = reinterpret_cast<int*>(w);
+  {
+    const size_t heads = (size_t)p->B * p->Hq, groups = (size_t)p->B * p->Hkv;
+    unsigned* c = reinterpret_cast<unsigned*>(w + L.counters);
+    a->end_cnt = c;
+    a->grp_cnt = c + kSyncBytes / 4;
+    a->est_cnt = a->grp_cnt + groups;
+    a->head_cnt = a->est_cnt + groups;
+    a->sel_ready = a->head_cnt + heads;
+    a->neg_ready = a->sel_ready + heads;
+    a->counter_words = (int)(2 * groups + 3 * heads);
+  }
   a->scores = reinterpret_cast<float*>(w + L.scores);
   a->head_max = reinterpret_cast<float*>(w + L.head_max);
   a->sel_ids = reinterpret_cast<int*>(w + L.selected);
-  a->sel_prefix = reinterpret_cast<int*>(w + L.sel_prefix);
-  a->counters = reinterpret_cast<int*>(w + L.counters);
-  a->att_part = reinterpret_cast<float*>(w + L.att_partials);
-  a->est_part = reinterpret_cast<float*>(w + L.est_partials);
-  a->att_splits = L.att_splits;
-  a->est_chunks = L.est_chunks;
-  a->est_chunk_clusters = L.est_chunk_clusters;
+  a->sel_rows = reinterpret_cast<int*>(w + L.sel_rows);
+  a->sel_cnts = reinterpret_cast<int*>(w + L.sel_counts);
+  const size_t heads = (size_t)p->B * p->Hq, groups = (size_t)p->B * p->Hkv;
+  const size_t part = (size_t)wi::kPartStride * 4;
+  size_t off = L.partials;
+  a->est_part = reinterpret_cast<float*>(w + off);
+  off += align256((wi::kMaxBlocks + groups) * (size_t)a->G * part);
+  a->std_part = reinterpret_cast<float*>(w + off);
+  off += align256((wi::kMaxBlocks + heads) * part);
+  a->ret_part = reinterpret_cast<float*>(w + off);
+  off += align256((wi::kMaxBlocks + heads) * part);
+  a->neg_part = reinterpret_cast<float*>(w + off);
+  a->nb = nb;
+  a->tpg = tpg;
+  a->tph = (p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile;
+  // Blocks [0, nsel) select (heads dealt round robin); the others score the
+  // index tiles (a centroid-key and a value-sum tile each).  The split
+  // minimises the larger of the two loads, a selection costing about
+  // selection_weight() centroid-key tiles.
+  const long long H = (long long)p->B * p->Hq;
+  const double wsel = selection_weight(C);
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ns = 1; ns <= nb - 1 && ns <= H; ++ns) {
+    const double sel = (double)((H + ns - 1) / ns) * wsel;
+    const double idx = 2.0 * (double)((n_tiles + (nb - ns) - 1) / (nb - ns));
+    const double cost = sel > idx ? sel : idx;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = ns;
+    }
+  }
+  a->nsel = best;
   return WI_OK;
+}
+
+int run_decode(const wi_decode_params* p, const void* q, const void* K, const void* V,
+               const wi_index* index, float* out, float* lse, int32_t* topk_ids, void* workspace,
+               size_t workspace_bytes, wi_stream_t stream, int stages, bool need_q, bool need_kv) {
+  if ((stages & wi::kStageAttend) && out == nullptr) return WI_ERR_INVALID_ARG;
+  if (need_q && !need_kv) {
+    if (q == nullptr) return WI_ERR_INVALID_ARG;
+    if (!aligned(q, 16)) return WI_ERR_ALIGNMENT;
+  }
+  DecodeArgs a;
+  const int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_kv);
+  if (st != WI_OK) return st;
+  a.stages = stages;
+  a.fused = stages == (wi::kStageScore | wi::kStageSelect | wi::kStageAttend) ? 1 : 0;
+  a.out = out;
+  a.lse = lse;
+  a.topk_out = topk_ids;
+  if (stages & wi::kStageAttend) a.inject = g_inject.exchange(0);
+  return cuda_status(wi::launch_decode(a, (cudaStream_t)stream));
 }
 
 }  // namespace
@@ -365,57 +430,28 @@ int wi_decode_workspace_layout(const wi_decode_params* p, int n_clusters,
 
 int wi_decode_score(const wi_decode_params* p, const void* q, const wi_index* index,
                     void* workspace, size_t workspace_bytes, wi_stream_t stream) {
-  DecodeArgs a;
-  int st = fill_decode_args(p, q, nullptr, nullptr, index, workspace, workspace_bytes, &a, false);
-  if (st != WI_OK) return st;
-  if (q == nullptr) return WI_ERR_INVALID_ARG;
-  if (!aligned(q, 16)) return WI_ERR_ALIGNMENT;
-  if ((st = device_ok()) != WI_OK) return st;
-  return cuda_status(wi::launch_decode_score(a, (cudaStream_t)stream));
+  return run_decode(p, q, nullptr, nullptr, index, nullptr, nullptr, nullptr, workspace,
+                    workspace_bytes, stream, wi::kStageScore, true, false);
 }
 
 int wi_decode_select(const wi_decode_params* p, const wi_index* index, int32_t* topk_ids,
                      void* workspace, size_t workspace_bytes, wi_stream_t stream) {
-  DecodeArgs a;
-  int st = fill_decode_args(p, nullptr, nullptr, nullptr, index, workspace, workspace_bytes, &a,
-                            false);
-  if (st != WI_OK) return st;
-  if ((st = device_ok()) != WI_OK) return st;
-  a.topk_out = topk_ids;
-  return cuda_status(wi::launch_decode_select(a, (cudaStream_t)stream));
+  return run_decode(p, nullptr, nullptr, nullptr, index, nullptr, nullptr, topk_ids, workspace,
+                    workspace_bytes, stream, wi::kStageSelect, false, false);
 }
 
 int wi_decode_attend(const wi_decode_params* p, const void* q, const void* K, const void* V,
                      const wi_index* index, float* out, float* lse, void* workspace,
                      size_t workspace_bytes, wi_stream_t stream) {
-  DecodeArgs a;
-  int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, true);
-  if (st != WI_OK) return st;
-  if (out == nullptr) return WI_ERR_INVALID_ARG;
-  if ((st = device_ok()) != WI_OK) return st;
-  a.out = out;
-  a.lse = lse;
-  a.inject = g_inject.exchange(0);
-  return cuda_status(wi::launch_decode_attend(a, (cudaStream_t)stream));
+  return run_decode(p, q, K, V, index, out, lse, nullptr, workspace, workspace_bytes, stream,
+                    wi::kStageAttend, true, true);
 }
 
 int wi_decode_attention(const wi_decode_params* p, const void* q, const void* K, const void* V,
                         const wi_index* index, float* out, float* lse, int32_t* topk_ids,
                         void* workspace, size_t workspace_bytes, wi_stream_t stream) {
-  DecodeArgs a;
-  int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, true);
-  if (st != WI_OK) return st;
-  if (out == nullptr) return WI_ERR_INVALID_ARG;
-  if ((st = device_ok()) != WI_OK) return st;
-  a.out = out;
-  a.lse = lse;
-  a.topk_out = topk_ids;
-  a.inject = g_inject.exchange(0);
-  const cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = wi::launch_decode_score(a, s);
-  if (e == cudaSuccess) e = wi::launch_decode_select(a, s);
-  if (e == cudaSuccess) e = wi::launch_decode_attend(a, s);
-  return cuda_status(e);
+  return run_decode(p, q, K, V, index, out, lse, topk_ids, workspace, workspace_bytes, stream,
+                    wi::kStageScore | wi::kStageSelect | wi::kStageAttend, true, true);
 }
 
 int wi_sync_status(void* workspace, wi_stream_t stream, int* device_status) {

@@ -1,27 +1,45 @@
-// Decode kernels of the wave-index tripartite attention ("RetroInfer: A Vector
+// Decode kernel of the wave-index tripartite attention ("RetroInfer: A Vector
 // Storage Engine for Scalable Long-Context LLM Inference", technical summary
 // (es) §2.A: steady zone, retrieval zone, estimation zone; technical summary
-// (ar) §2.a: estimation from centroids and the value sum, §2.b: retrieved KV
-// laid out contiguously).  Three launches, chained with programmatic
-// dependent launch:
+// (ar) §2.a: estimation from the centroids and the value sum, §2.b: retrieved
+// KV laid out contiguously for the attention kernel).
 //
-//   score_kernel   s[b,h,c] = scale q_h . kbar_c (-inf if empty): one pass over
-//                  the f32 centroid keys, one warp per 512-byte row, 128-bit
-//                  loads, all query heads of a KV group per pass.
-//   select_kernel  two block roles in one launch, so that the selection's
-//                  latency hides under the value-sum stream:
-//                  (a) per query head, radix select of the r largest scores
-//                      (order: score desc, id asc): ids ascending + token prefix;
-//                  (b) per chunk of clusters of one KV head, the estimate of
-//                      EVERY non-empty cluster: (m, l = sum n_c e^{s_c-m},
-//                      o = sum e^{s_c-m} vsum_c).
-//   attend_kernel  per (query head, split of its token list): exact attention
-//                  over the steady zone and the retrieved clusters, rows staged
-//                  into shared memory by the TMA bulk-copy engine (cp.async.bulk
-//                  + mbarrier, double buffered); the same block emits the
-//                  retrieved clusters' estimates with a negative sign, so that
-//                  all-minus-retrieved is the estimation zone; the last block of
-//                  a head merges every partial (log-sum-exp) into out and lse.
+// One persistent launch, one block per SM.  Each block has 16 consumer warps
+// and one producer warp.  The producer streams every byte the block needs
+// through a 4-stage shared-memory ring with the TMA bulk-copy engine
+// (cp.async.bulk + mbarrier complete_tx); the consumers compute on the staged
+// tiles.  Blocks [0, nsel) are selection blocks, the others scoring blocks.
+//
+//   stage 1  (scoring blocks) centroid-key tiles (64 rows of kbar, f32) with
+//            the group's query rows, in KV-group order, dealt round robin:
+//              s[b,h,c] = scale q_h . kbar_c (-inf if n_c = 0)   -> scores
+//            every warp counts its finished tiles on the group's counter;
+//   stage 2  (selection blocks) once a head's group is fully scored: radix
+//            select of the r largest scores (score desc, id asc), the selected
+//            clusters' sorted rows and sizes; afterwards the estimate of the
+//            selected clusters with a negative sign (all-minus-retrieved is the
+//            estimation zone);
+//            (scoring blocks) value-sum tiles of a contiguous share of the
+//            clusters: the estimate of EVERY non-empty cluster, (m, l = sum n_c
+//            e^{s_c-m}, o = sum e^{s_c-m} vsum_c), one partial per (block, KV
+//            group, query head);
+//   stage 3  (all blocks) steady-zone tiles (K/V rows of the sink and the local
+//            window) and retrieved-cluster tiles (K/V rows of the
+//            cluster-sorted copies, streamed once the head's selection is
+//            published), exact attention with an online softmax; every
+//            finished piece adds itself to its head's arrival counter and the
+//            block that completes a head merges all of its partials
+//            (log-sum-exp) into out and lse.
+//
+// There is no grid-wide barrier: each consumer of another block's results
+// waits on a counter of exactly what it reads (a KV group's scores, a head's
+// selection, a group's estimate pieces, a head's negative estimate), so the
+// selections of early groups overlap the scoring of later ones and the
+// streaming of value sums and steady rows.  The counters start at zero; the
+// last block to finish a launch clears them again.  Every wait is bounded
+// (kWaitLimitNs) and reports WI_ERR_DEVICE_TIMEOUT; a block that gives up lets
+// its issued copies land before it exits.
+//
 // Softmax quantities are kept in log2 units (logits scaled by log2 e) so that
 // every exponential is an exp2.
 #include <float.h>
@@ -35,99 +53,244 @@ namespace wi {
 
 namespace {
 
-template <typename... KArgs, typename... Args>
-cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                      cudaStream_t st, bool pdl, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+constexpr int kCW = 16;                       // consumer warps
+constexpr int kCT = kCW * 32;                 // consumer threads
+constexpr int kThreads = kCT + 32;            // + one producer warp
+constexpr int kStages = 4;
+constexpr int kTile = kDecodeTile;            // index rows or tokens per tile
+constexpr int kRowsPerWarp = kTile / kCW;     // 4
+constexpr uint32_t kStageBytes = kTile * 512; // 64 f32 rows, or 64 K + 64 V bf16 rows
+constexpr int kQSlotBytes = 8 * kD * 2;       // up to 8 bf16 query rows
+constexpr int kBins = 4096;                   // radix-select histogram (12-bit digits)
+constexpr int kCand = 1024;                   // selected clusters kept in shared memory
+constexpr int kSelChunk = kCT * 16;           // keys per register chunk (16 per thread)
+// candidate windows below the largest key, in 12-bit key digits (8 per octave)
+constexpr int kNumWindows = 8;
+__host__ __device__ constexpr uint32_t window_digits(int w) { return 2u * (w + 1); }  // 2, 4, ..., 16
+static_assert(kRowsPerWarp == 4, "tile layout");
+
+enum : int { kTileEnd = 0, kTileSteady = 1, kTileRet = 2, kTileIndex = 3 };
+
+struct TileInfo {
+  int kind, bh, ntok, last, units, pad0, pad1, pad2;
+};
+
+struct Cand {
+  int c[kCand];
+  float s[kCand];
+  int n[kCand];
+  int row[kCand];
+};
+
+// Per-warp side data of one index tile (sizes of the warp's 4 rows; their
+// scores for each head of the group), fetched with cp.async kSideAhead tiles ahead.
+struct __align__(16) SideSlot {
+  int n[4];
+  float s[8][4];
+};
+constexpr int kSideSlots = 8;  // prefetch distance kSideSlots - 2 tiles
+constexpr int kSideAhead = kSideSlots - 2;
+
+struct __align__(128) DecSmem {
+  unsigned char ring[kStages][kStageBytes];  // bulk-copy destinations (16-byte aligned)
+  SideSlot side[kCW][kSideSlots];
+  unsigned char qs[kStages][kQSlotBytes];
+  float red_o[kCW][kD];
+  float red_m[kCW];
+  float red_l[kCW];
+  union __align__(16) {
+    int hist[kBins];
+    Cand cand;
+    float w[kBins];
+  } u;
+  unsigned long long full[kStages];
+  unsigned long long empty[kStages];
+  TileInfo info[kStages];
+  int2 scan[2][kCW];
+  int sel_i[4];
+  uint32_t red_u[2][kCW];
+  uint32_t sel_hand[8];
+  uint32_t win_sum[2][kCW][kNumWindows / 2];
+  int abort;              // some wait of this block gave up
+  int issued;             // tiles whose copies the producer issued
+  int confirmed;          // tiles whose full barrier the consumers saw complete
+  int flag;
+};
+static_assert(offsetof(DecSmem, qs) % 16 == 0, "bulk-copy alignment");
+static_assert(offsetof(DecSmem, red_o) % 16 == 0, "float4 alignment");
+static_assert(offsetof(DecSmem, full) % 8 == 0, "mbarrier alignment");
+static_assert(offsetof(DecSmem, u) % 16 == 0, "scratch union alignment");
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-
-// --------------------------------------------------------------------------
-// K1: centroid scoring
-// --------------------------------------------------------------------------
-constexpr int kScoreThreads = 256;
-constexpr int kScoreWarps = kScoreThreads / 32;
-
-template <int G>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(DecodeArgs a, int rows_per_block,
-                                                              int blocks_per_head) {
-  grid_dep_launch();
-  grid_dep_wait();
-  constexpr int ROWS = 32 / G;  // rows per transpose-reduce batch
-  constexpr int NB = ROWS >= 16 ? 1 : 2;  // batches in flight: 8-32 rows per warp
-  const int bg = blockIdx.x / blocks_per_head;
-  const int chunk = blockIdx.x - bg * blocks_per_head;
-  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-  float4 qv[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint2 w =
-        reinterpret_cast<const uint2*>(a.q + ((size_t)b * a.Hq + g * G + h) * kD)[lane];
-    qv[h] = make_float4(bf_lo(w.x) * a.scale, bf_hi(w.x) * a.scale, bf_lo(w.y) * a.scale,
-                        bf_hi(w.y) * a.scale);
-  }
-  const float4* kb = reinterpret_cast<const float4*>(a.kbar + (size_t)bg * a.C * kD);
-  const int* sz = a.size + (size_t)bg * a.C;
-  const int c_begin = chunk * rows_per_block;
-  const int c_end = min(a.C, c_begin + rows_per_block);
-  for (int c0 = c_begin + warp * NB * ROWS; c0 < c_end; c0 += kScoreWarps * NB * ROWS) {
-    float4 kv[NB * ROWS];
-#pragma unroll
-    for (int r = 0; r < NB * ROWS; ++r) {
-      const int c = c0 + r;
-      kv[r] = (c < c_end) ? __ldg(kb + (size_t)c * (kD / 4) + lane)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      float v[32];
-#pragma unroll
-      for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 k4 = kv[nb * ROWS + r];
-          v[r * G + h] = k4.x * qv[h].x + k4.y * qv[h].y + k4.z * qv[h].z + k4.w * qv[h].w;
-        }
-      const float tot = warp_transpose_sum32(v, lane);
-      const int r = lane / G, h = lane - (lane / G) * G;
-      const int c = c0 + nb * ROWS + r;
-      if (c < c_end) {
-        const int n = __ldg(sz + c);
-        a.scores[((size_t)b * a.Hq + g * G + h) * a.C + c] = n > 0 ? tot : -INFINITY;
-      }
-    }
-  }
+// Named barrier 1 over the 512 consumer threads (the producer warp never
+// takes part).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// Named barrier 1 with an OR-reduction of a predicate over the consumers.
+__device__ __forceinline__ bool cany(bool x) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 512, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)x)
+      : "memory");
+  return r != 0;
 }
-
-// --------------------------------------------------------------------------
-// K2: selection (role a) and estimation over all clusters (role b)
-// --------------------------------------------------------------------------
-constexpr int kK2Threads = 512;
-constexpr int kK2Warps = kK2Threads / 32;
-constexpr int kSelCacheMax = 16384;              // keys kept in shared memory up to this C
-constexpr int kEstBatch = kEstChunk / kK2Warps;  // clusters per warp: 16
-static_assert(kEstBatch == 16, "estimation batch layout");
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ uint2 lds2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+// Asynchronous global -> shared copies (cp.async): unlike plain loads, they
+// are not waited for by warp or block barriers, only by cp_async_wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   return (s == -INFINITY) ? 0u : float_key(s);  // 0 <=> empty cluster
 }
 
-// Exclusive scan of an int pair over the block; returns the prefix and the
-// block total in *total.  sh must hold 33 entries.
-__device__ __forceinline__ int2 block_scan2(int2 v, int2* sh, int2* total) {
+// Progress counters: a count that only grows within a launch.  Writers make
+// their results visible (every writing thread fences, then a barrier) before
+// one thread adds to the count; a reader waits (acquire) until the count
+// reaches what it needs.
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *cnt >= target; gives up early once *abort is set.
+__device__ __noinline__ bool count_wait(const unsigned* cnt, unsigned target, int* status,
+                                        const int* abort) {
+  if (ld_acquire(cnt) >= target) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (ld_acquire(cnt) >= target) return true;
+    if (*(volatile const int*)abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      report(status, WI_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Reduce-scatter of V = 4G per-lane values: afterwards lane L holds the sum
+// over all 32 lanes of value index (L mod V).
+template <int V>
+__device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
+#pragma unroll
+  for (int off = V / 2; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (int off = V; off < 32; off <<= 1) x += __shfl_xor_sync(kFull, x, off);
+  return x;
+}
+
+// Block-range helpers for the uniform partitions: block b of nb owns
+// [b*len/nb, (b+1)*len/nb).
+__device__ __forceinline__ long long part_lo(long long b, long long len, int nb) {
+  return b * len / nb;
+}
+__device__ __forceinline__ int part_owner(long long p, long long len, int nb) {
+  return (int)(((p + 1) * nb - 1) / len);
+}
+
+struct Sched {
+  bool sel;                    // a selection block
+  int sel0, sel_step;          // its heads sel0, sel0 + sel_step, ... < B*Hq
+  int kj, nk, n1;              // scoring block kj of nk: centroid-key tiles kj + i*nk, i < n1
+  int v0, v1;                  // its value-sum tiles [v0, v1)
+  long long s0, s1;            // steady tiles
+  long long r0, r1;            // retrieved slots
+};
+
+__device__ Sched schedule(const DecodeArgs& a, int b) {
+  Sched s;
+  const long long nt = (long long)a.B * a.Hkv * a.tpg;
+  s.sel = b < a.nsel;
+  s.sel0 = b;
+  s.sel_step = a.nsel;
+  s.nk = a.nb - a.nsel;
+  s.kj = b - a.nsel;
+  s.n1 = 0;
+  s.v0 = s.v1 = 0;
+  if (!s.sel) {
+    s.n1 = s.kj < nt ? (int)((nt - s.kj + s.nk - 1) / s.nk) : 0;
+    s.v0 = (int)part_lo(s.kj, nt, s.nk);
+    s.v1 = (int)part_lo(s.kj + 1, nt, s.nk);
+  }
+  const long long nst = (long long)a.B * a.Hq * a.tph;
+  s.s0 = part_lo(b, nst, a.nb);
+  s.s1 = part_lo(b + 1, nst, a.nb);
+  const long long nr = (long long)a.B * a.Hq * a.r;
+  s.r0 = part_lo(b, nr, a.nb);
+  s.r1 = part_lo(b + 1, nr, a.nb);
+  return s;
+}
+
+// Combine the 16 consumer warps' (m, l, o) into one partial at dst:
+// dst[0] = m (log2 units), dst[1] = sign * l, dst[2..] = sign * o.
+// m and l are warp-uniform; o holds this lane's 4 dimensions.  The writing
+// threads fence before the closing barrier, so that one thread may publish the
+// partial with a counter right after it.
+__device__ void combine_write(DecSmem& S, float m, float l, float4 o, float* dst, float sign) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) {
+    S.red_m[warp] = m;
+    S.red_l[warp] = l;
+  }
+  reinterpret_cast<float4*>(S.red_o[warp])[lane] = o;
+  csync();
+  if (tid < kD) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) M = fmaxf(M, S.red_m[w]);
+    float L = 0.f, O = 0.f;
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kCW; ++w) {
+        const float mw = S.red_m[w];
+        const float f = mw > -INFINITY ? exp2f(mw - M) : 0.f;
+        L += S.red_l[w] * f;
+        O += S.red_o[w][tid] * f;
+      }
+    }
+    if (tid == 0) {
+      dst[0] = (L > 0.f) ? M : -INFINITY;
+      dst[1] = sign * L;
+    }
+    dst[2 + tid] = sign * O;
+    fence_gpu();
+  }
+  csync();
+}
+
+// Exclusive scan of an int2 over the 512 consumers; *total gets the sum.  One
+// named barrier: the two halves of S.scan alternate between calls (`buf`),
+// and every call's barrier separates a half's reads from its next write.
+__device__ int2 cscan2(int2 v, DecSmem& S, int2* total, int& buf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
   int2 incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -138,697 +301,1388 @@ __device__ __forceinline__ int2 block_scan2(int2 v, int2* sh, int2* total) {
       incl.y += y;
     }
   }
+  int2* sh = S.scan[buf];
+  buf ^= 1;
   if (lane == 31) sh[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int2 w = lane < nwarps ? sh[lane] : make_int2(0, 0);
-    int2 wi = w;
+  csync();
+  int2 base = make_int2(0, 0), tot = make_int2(0, 0);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(kFull, wi.x, o);
-      const int y = __shfl_up_sync(kFull, wi.y, o);
-      if (lane >= o) {
-        wi.x += x;
-        wi.y += y;
-      }
+  for (int w = 0; w < kCW; ++w) {
+    const int2 t = sh[w];
+    if (w < warp) {
+      base.x += t.x;
+      base.y += t.y;
     }
-    sh[lane] = make_int2(wi.x - w.x, wi.y - w.y);
-    if (lane == 31) sh[32] = wi;
+    tot.x += t.x;
+    tot.y += t.y;
   }
-  __syncthreads();
-  const int2 base = sh[warp];
-  *total = sh[32];
-  const int2 res = make_int2(base.x + incl.x - v.x, base.y + incl.y - v.y);
-  __syncthreads();  // sh may be reused by the caller
-  return res;
+  *total = tot;
+  return make_int2(base.x + incl.x - v.x, base.y + incl.y - v.y);
 }
 
-struct SelShared {
-  int hist[256];
-  int2 scan[33];
-  int i[8];
-  uint32_t u[32];
-};
-
-// Role (a): the r_eff = min(r, non-empty) largest scores of one query head.
-// Radix select on order-preserving keys, 8 bits per pass, histograms built
-// with warp-aggregated shared atomics; stops as soon as the boundary bin is
-// taken whole.  Equal keys at the boundary keep the lowest ids.
-__device__ void select_head(const DecodeArgs& a, int bh, uint32_t* skey, SelShared& S,
-                            int cached) {
+// ---------------------------------------------------------------------------
+// The r-th largest of n <= kCT distinct 64-bit values v[0..n) in shared
+// memory (1 <= r <= n), by all consumer threads (thread t holds v[t]): radix
+// select with 11-bit digits from the highest bit in which the values differ;
+// histograms of 2048 counters in `hist` (shared), boundary digit by a block
+// scan.  About two passes for values that differ in their top bits.
+__device__ unsigned long long block_select_desc(DecSmem& S, const unsigned long long* v, int n,
+                                                int r, int* hist, int& buf) {
+  constexpr int kDig = 11, kNb = 1 << kDig, kPer = kNb / kCT;  // 4 digits per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / a.G;
-  const int C = a.C;
-  const float* sc = a.scores + (size_t)bh * C;
-  const int* sz = a.size + ((size_t)b * a.Hkv + g) * C;
-  auto key = [&](int c) -> uint32_t { return cached ? skey[c] : score_key(__ldcg(sc + c)); };
-
-  int valid = 0;
-  uint32_t kmax = 0;
-  for (int c = tid; c < C; c += kK2Threads) {
-    const uint32_t k = score_key(__ldcg(sc + c));
-    if (cached) skey[c] = k;
-    valid += (k != 0);
-    kmax = max(kmax, k);
+  const bool has = tid < n;
+  const unsigned long long mine = has ? v[tid] : 0ull, v0 = v[0];
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(S.red_o[0]);  // [2][kCW][2]
+  auto block_or_min = [&](unsigned long long x, unsigned long long y, unsigned long long& xo,
+                          unsigned long long& yo) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      x |= __shfl_xor_sync(kFull, x, o);
+      const unsigned long long t = __shfl_xor_sync(kFull, y, o);
+      y = t < y ? t : y;
+    }
+    unsigned long long* rb = red + (size_t)buf * 2 * kCW;
+    buf ^= 1;
+    if (lane == 0) {
+      rb[2 * warp] = x;
+      rb[2 * warp + 1] = y;
+    }
+    csync();
+    xo = 0ull;
+    yo = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+      xo |= rb[2 * w];
+      yo = rb[2 * w + 1] < yo ? rb[2 * w + 1] : yo;
+    }
+  };
+  unsigned long long diff, lo;
+  block_or_min(has ? (mine ^ v0) : 0ull, has ? mine : ~0ull, diff, lo);
+  if (r == n || diff == 0ull) return lo;  // every value taken
+  int bit = 63 - __clzll(diff);
+  unsigned long long mask = bit == 63 ? 0ull : (~0ull << (bit + 1));
+  unsigned long long prefix = v0 & mask;
+  int remaining = r;
+  uint32_t* hand = S.sel_hand;
+  for (int pass = 0;; ++pass) {
+    const int width = min(kDig, bit + 1), shift = bit + 1 - width;
+    const unsigned long long dm = (1ull << width) - 1ull;
+    const int nbins = 1 << width;
+    for (int i = tid; i < nbins; i += kCT) hist[i] = 0;
+    csync();
+    if (has && (mine & mask) == prefix) atomicAdd(&hist[(int)((mine >> shift) & dm)], 1);
+    csync();
+    // thread t owns the kPer digits [hi - kPer, hi) counted from the top
+    const int bhi = nbins - kPer * tid, blo = max(0, bhi - kPer);
+    int own = 0;
+    if (bhi > 0)
+      for (int i = blo; i < bhi; ++i) own += hist[i];
+    int2 tot;
+    const int excl = cscan2(make_int2(own, 0), S, &tot, buf).x;
+    uint32_t* hd = hand + 2 * (pass & 1);  // hand[0..1] / hand[2..3], alternating
+    if (own > 0 && excl < remaining && remaining <= excl + own) {
+      int acc = excl;
+      for (int i = bhi - 1; i >= blo; --i) {
+        const int c = hist[i];
+        if (acc + c >= remaining) {
+          hd[0] = (uint32_t)i | ((uint32_t)c << 16);
+          hd[1] = (uint32_t)acc;
+          break;
+        }
+        acc += c;
+      }
+    }
+    csync();
+    const int D = (int)(hd[0] & 0xffffu), cntD = (int)(hd[0] >> 16), above = (int)hd[1];
+    remaining -= above;
+    prefix |= (unsigned long long)D << shift;
+    mask |= dm << shift;
+    if (cntD == remaining || shift == 0) {
+      // every value of the boundary digit is taken: the smallest of them
+      unsigned long long dummy, m;
+      block_or_min(0ull, (has && (mine & mask) == prefix) ? mine : ~0ull, dummy, m);
+      return m;
+    }
+    bit = shift - 1;
   }
+}
+
+// ---------------------------------------------------------------------------
+// selection of one query head (all 512 consumers)
+// ---------------------------------------------------------------------------
+// T = the r_eff = min(r, non-empty) largest scores, ties to the lower id.  T is
+// found as a threshold on (key, id): a cluster with order-preserving key k is
+// selected iff k > Kb, or k == Kb and its id <= cb.  Keys are held in
+// registers, 16 consecutive ids per thread.  One pass histograms the keys'
+// top 12 bits (4096 digits; a larger key never has a smaller digit); the digit
+// D holding the r_eff-th largest key follows from a scan from the top, every
+// cluster with a larger digit is selected, and the candidates with digit D are
+// ranked exactly by (key desc, id asc) to give (Kb, cb).  When digit D holds
+// more than kCand candidates an exact radix select over the keys gives
+// (Kb, cb) instead.  The selected ids are compacted in ascending order; one
+// round of independent loads then fetches each cluster's size, first sorted
+// row and value-sum row for the outputs and for the estimate of T (kept with
+// a negative sign).
+template <int G>
+__device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / G;
+  const size_t bg = (size_t)b * a.Hkv + g;
+  const int C = a.C, r = a.r, rs = r > 0 ? r : 1;
+  const float* sc = a.scores + (size_t)bh * C;
+  const int* sz = a.size + bg * C;
+  const int* off = a.offset + bg * (C + 1);
+  const int nch = (C + kSelChunk - 1) / kSelChunk;
+  const bool vec = (C & 3) == 0;  // rows of scores start on 16-byte boundaries
+  int buf = 0;
+
+  auto load16 = [&](int ch, uint32_t(&k)[16]) {
+    const int c0 = ch * kSelChunk + tid * 16;
+    if (vec && c0 + 16 <= C) {
+      const float4* p = reinterpret_cast<const float4*>(sc + c0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 f = __ldcg(p + j);
+        k[4 * j] = score_key(f.x);
+        k[4 * j + 1] = score_key(f.y);
+        k[4 * j + 2] = score_key(f.z);
+        k[4 * j + 3] = score_key(f.w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) k[j] = (c0 + j < C) ? score_key(__ldcg(sc + c0 + j)) : 0u;
+    }
+  };
+  uint32_t k0[16];
+  load16(0, k0);
+  // f(key, id) over this thread's keys
+  auto visit = [&](auto&& f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f(k0[j], tid * 16 + j);
+    for (int ch = 1; ch < nch; ++ch) {
+      uint32_t kk[16];
+      load16(ch, kk);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) f(kk[j], ch * kSelChunk + tid * 16 + j);
+    }
+  };
+
+  // non-empty count and key range
+  int valid = 0;
+  uint32_t kmax = 0u, kmin = 0xffffffffu;
+  visit([&](uint32_t k, int) {  // branch-free: selects, no divergent jumps
+    valid += (int)(k != 0u);
+    kmax = max(kmax, k);
+    kmin = min(kmin, k != 0u ? k : 0xffffffffu);
+  });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     valid += __shfl_xor_sync(kFull, valid, o);
     kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
   }
-  if (lane == 0) {
-    S.scan[warp].x = valid;
-    S.u[warp] = kmax;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < kK2Warps ? S.scan[lane].x : 0;
-    uint32_t m = lane < kK2Warps ? S.u[lane] : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      v += __shfl_xor_sync(kFull, v, o);
-      m = max(m, __shfl_xor_sync(kFull, m, o));
-    }
+  uint32_t* hand = S.sel_hand;
+  {
+    int2* sh = S.scan[buf];
+    buf ^= 1;
     if (lane == 0) {
-      S.i[0] = v;
-      S.i[5] = (int)m;
+      sh[warp] = make_int2(valid, 0);
+      S.red_u[0][warp] = kmax;
+      S.red_u[1][warp] = kmin;
+    }
+    if (tid == 0) hand[3] = 0u;  // candidate counter
+    csync();
+    valid = 0;
+    kmax = 0u;
+    kmin = 0xffffffffu;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+      valid += sh[w].x;
+      kmax = max(kmax, S.red_u[0][w]);
+      kmin = min(kmin, S.red_u[1][w]);
     }
   }
-  __syncthreads();
-  valid = S.i[0];
-  kmax = (uint32_t)S.i[5];
-  const int r = a.r;
   const int r_eff = min(r, valid);
   if (tid == 0) a.head_max[bh] = valid > 0 ? key_float(kmax) : -INFINITY;
 
-  uint32_t prefix = 0, mask = 0;
-  int remaining = r_eff, count = 0;
-  if (r_eff > 0) {
+  // threshold (Kb, cb); the default selects nothing
+  uint32_t Kb = 0xffffffffu;
+  int cb = -1;
+  if (r_eff > 0 && r_eff == valid) {
+    Kb = 0u;  // every non-empty cluster
+  } else if (r_eff > 0) {
+    bool done = false;
+    int win = -1, win_total = 0;
+    // Candidates: keys whose top 12 bits (d = k >> 20) lie within w digits of
+    // the largest key's, d_max - d <= w, for the smallest w of 2, 4, ..., 16 that
+    // holds at least r_eff keys (one counting pass, all windows at once).  When
+    // they number at most kCT, a radix select over them finds the r_eff-th
+    // largest (key desc, id asc).
+    const uint32_t dmax = kmax >> 20;
+    // per-thread counts of the windows, one byte each (at most 16 keys): a
+    // key o digits below the largest is in windows w >= w0(o)
+    unsigned long long cw64 = 0ull;
+    visit([&](uint32_t k, int) {
+      const uint32_t o = dmax - (k >> 20);  // digits below the largest
+      const uint32_t w0 = o <= 2u ? 0u : min((o - 1u) >> 1, 8u);  // 8: in no window
+      const unsigned long long inc = w0 < 8u ? (0x0101010101010101ull << (8u * w0)) : 0ull;
+      cw64 += k != 0u ? inc : 0ull;
+    });
+    const uint32_t cw[2] = {(uint32_t)cw64, (uint32_t)(cw64 >> 32)};
+    {
+      // block totals (at most 8192 each): two 16-bit fields per word
+      uint32_t(*wsum)[kNumWindows / 2] =
+          reinterpret_cast<uint32_t(*)[kNumWindows / 2]>(S.win_sum[buf]);
+      buf ^= 1;
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) S.hist[tid] = 0;
-      __syncthreads();
-      for (int base = 0; base < C; base += kK2Threads) {
-        const int c = base + tid;
-        const uint32_t k = c < C ? key(c) : 0u;
-        const bool in = k != 0u && (k & mask) == prefix;
-        const int d = in ? (int)((k >> shift) & 0xffu) : 256 + lane;
-        const unsigned peers = __match_any_sync(kFull, d);
-        if (in && lane == __ffs(peers) - 1) atomicAdd(&S.hist[d], __popc(peers));
-      }
-      __syncthreads();
-      if (warp == 0) {
-        int cnt[8];
-        int tot = 0;
+      for (int x = 0; x < kNumWindows / 2; ++x) {
+        const uint32_t c = (x < 2 ? cw[0] : cw[1]) >> (16 * (x % 2));
+        uint32_t pk = (c & 0xffu) | ((c >> 8 & 0xffu) << 16);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          cnt[j] = S.hist[255 - 8 * lane - j];
-          tot += cnt[j];
+        for (int o = 16; o > 0; o >>= 1) pk += __shfl_xor_sync(kFull, pk, o);
+        if (lane == 0) wsum[warp][x] = pk;
+      }
+      csync();
+#pragma unroll 1
+      for (int x = kNumWindows / 2 - 1; x >= 0; --x) {
+        uint32_t t = 0u;
+#pragma unroll
+        for (int y = 0; y < kCW; ++y) t += wsum[y][x];
+        const int hi = (int)(t >> 16), lo = (int)(t & 0xffffu);  // windows 2x+1, 2x
+        if (hi >= r_eff) {
+          win = 2 * x + 1;
+          win_total = hi;
         }
-        int incl = tot;
+        if (lo >= r_eff) {
+          win = 2 * x;
+          win_total = lo;
+        }
+      }
+    }
+    const uint32_t wsel = win >= 0 ? window_digits(win) : 0u;
+    int nc = 0;
+#pragma unroll
+    for (int w = 0; w < kNumWindows; ++w)
+      if (w == win) nc = (int)((cw[w / 4] >> (8 * (w % 4))) & 0xffu);
+    auto in_window = [&](uint32_t k) { return k != 0u && dmax - (k >> 20) <= wsel; };
+    // candidates as composites (key << 32 | ~id): larger composite = selected
+    // first; unique since ids are
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(S.u.hist);
+    int2 ctot;
+    int cpos = cscan2(make_int2(nc, 0), S, &ctot, buf).x;
+    const int n_cand = win >= 0 ? win_total : 0;
+    if (n_cand >= r_eff && n_cand <= kCT) {
+      visit([&](uint32_t k, int c) {
+        if (in_window(k))
+          cand[cpos++] = ((unsigned long long)k << 32) | (unsigned long long)(0xffffffffu - (uint32_t)c);
+      });
+      csync();
+      const unsigned long long T = block_select_desc(S, cand, n_cand, r_eff,
+                                                     reinterpret_cast<int*>(cand + kCT), buf);
+      Kb = (uint32_t)(T >> 32);
+      cb = (int)(0xffffffffu - (uint32_t)T);
+      done = true;
+    }
+    if (!done) {
+      // exact radix select over the keys, 12 bits per pass from the highest
+      // bit in which they differ
+      int remaining = r_eff;
+      uint32_t prefix = 0u, mask = 0u;
+      bool tie = false;
+      if (kmax == kmin) {
+        prefix = kmax;
+        mask = 0xffffffffu;
+        tie = true;
+      } else {
+        int bit = 31 - __clz(kmax ^ kmin);
+        mask = (bit == 31) ? 0u : (0xffffffffu << (bit + 1));
+        prefix = kmax & mask;
+        for (int pass = 0;; ++pass) {
+          const int width = min(12, bit + 1), shift = bit + 1 - width;
+          const uint32_t dmask = (1u << width) - 1u;
+          const int nbins = 1 << width;
+          for (int i = tid; i < nbins; i += kCT) S.u.hist[i] = 0;
+          csync();
+          const uint32_t pf = prefix, mk = mask;
+          visit([&](uint32_t k, int) {
+            if (k != 0u && (k & mk) == pf) atomicAdd(&S.u.hist[(k >> shift) & dmask], 1);
+          });
+          csync();
+          const int bhi = nbins - 8 * tid, blo = max(0, bhi - 8);
+          int own = 0;
+          if (bhi > 0)
+            for (int i = blo; i < bhi; ++i) own += S.u.hist[i];
+          int2 tot;
+          const int excl = cscan2(make_int2(own, 0), S, &tot, buf).x;
+          uint32_t* hand = S.red_u[pass & 1];
+          if (own > 0 && excl < remaining && remaining <= excl + own) {
+            int acc = excl;
+            for (int i = bhi - 1; i >= blo; --i) {
+              const int cnt = S.u.hist[i];
+              if (acc + cnt >= remaining) {
+                hand[0] = (uint32_t)i;
+                hand[1] = (uint32_t)acc;
+                hand[2] = (uint32_t)cnt;
+                break;
+              }
+              acc += cnt;
+            }
+          }
+          csync();
+          const int D = (int)hand[0], above = (int)hand[1], cntD = (int)hand[2];
+          remaining -= above;
+          prefix |= (uint32_t)D << shift;
+          mask |= dmask << shift;
+          if (cntD == remaining) break;  // the boundary bin is taken whole
+          if (shift == 0) {              // equal full keys straddle the boundary
+            tie = true;
+            break;
+          }
+          bit = shift - 1;
+        }
+      }
+      if (!tie) {
+        // (k & mask) >= prefix  <=>  k >= prefix
+        Kb = prefix > 0u ? prefix - 1u : 0u;
+        cb = -1;
+      } else {
+        // k > prefix, plus the `remaining` lowest ids with k == prefix
+        Kb = prefix;
+        int eq_base = 0;
+        for (int ch = 0; ch < nch; ++ch) {
+          uint32_t kk[16];
+          if (ch == 0) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) kk[j] = k0[j];
+          } else {
+            load16(ch, kk);
+          }
+          int ne = 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ne += (kk[j] == prefix);
+          int2 tot;
+          const int before = eq_base + cscan2(make_int2(ne, 0), S, &tot, buf).x;
+          eq_base += tot.x;
+          if (before < remaining && remaining <= before + ne) {
+            int x = before;
+            for (int j = 0; j < 16; ++j) {
+              if (kk[j] == prefix && ++x == remaining) {
+                S.red_u[1][2] = (uint32_t)(ch * kSelChunk + tid * 16 + j);
+                break;
+              }
+            }
+          }
+        }
+        csync();
+        cb = (int)S.red_u[1][2];
+      }
+    }
+  }
+
+  // ordered compaction (ids ascending) into shared memory and the id outputs
+  int* ids = a.sel_ids + (size_t)bh * rs;
+  int* rows = a.sel_rows + (size_t)bh * rs;
+  int* cnts = a.sel_cnts + (size_t)bh * rs;
+  int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
+  int sel_base = 0;
+  if (r_eff > 0) {
+    for (int ch = 0; ch < nch; ++ch) {
+      uint32_t kk[16];
+      if (ch == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) kk[j] = k0[j];
+      } else {
+        load16(ch, kk);
+      }
+      const int c0 = ch * kSelChunk + tid * 16;
+      uint32_t selmask = 0u;
+      int nsel = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t k = kk[j];
+        if (k != 0u && (k > Kb || (k == Kb && c0 + j <= cb))) {
+          selmask |= 1u << j;
+          ++nsel;
+        }
+      }
+      int2 tot;
+      int pos = sel_base + cscan2(make_int2(nsel, 0), S, &tot, buf).x;
+      sel_base += tot.x;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if ((selmask & (1u << j)) && pos < r) {
+          const int c = c0 + j;
+          ids[pos] = c;
+          if (topk) topk[pos] = c;
+          if (pos < kCand) {
+            S.u.cand.c[pos] = c;
+            S.u.cand.s[pos] = key_float(kk[j]);
+          }
+          ++pos;
+        }
+      }
+    }
+  }
+  const int nsel_tot = min(sel_base, r);  // == r_eff
+  for (int i = nsel_tot + tid; i < rs; i += kCT) {
+    ids[i] = -1;
+    rows[i] = 0;
+    cnts[i] = 0;
+    if (topk && i < r) topk[i] = -1;
+  }
+  csync();
+
+  // the selected clusters' sizes and first sorted rows (one round of
+  // independent loads, 16 clusters per warp)
+  for (int j0 = warp * 32; j0 < nsel_tot; j0 += kCW * 32) {
+    const int j = j0 + lane;
+    if (j < nsel_tot) {
+      const int cj = j < kCand ? S.u.cand.c[j] : ids[j];
+      int nj = __ldg(sz + cj), rowj = __ldg(off + cj);
+      if (nj < 0 || rowj < 0 || (long long)rowj + nj > a.N_idx) {
+        report(a.status, WI_ERR_INDEX_MISMATCH);  // inconsistent index: stage nothing
+        nj = 0;
+        rowj = 0;
+      }
+      rows[j] = rowj;
+      cnts[j] = nj;
+    }
+  }
+  fence_gpu();  // the selection is published with a counter after this barrier
+  csync();
+}
+
+// The estimate of one head's selected clusters (kept with a negative sign):
+// (m, l = sum n_c e^{s_c - m}, o = sum e^{s_c - m} vsum_c) over T.  It reads
+// the selection outputs back (written by this block) and runs after the block
+// has published its selections.
+template <int G>
+__device__ void estimate_selected(const DecodeArgs& a, DecSmem& S, int bh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / G;
+  const size_t bg = (size_t)b * a.Hkv + g;
+  const int r = a.r, rs = r > 0 ? r : 1;
+  const int* ids = a.sel_ids + (size_t)bh * rs;
+  const int* cnts = a.sel_cnts + (size_t)bh * rs;
+  const float* sc = a.scores + (size_t)bh * a.C;
+  const float4* vs = reinterpret_cast<const float4*>(a.vsum + bg * (size_t)a.C * kD);
+  float m = -INFINITY, l = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = warp * 8; j0 < r; j0 += kCW * 8) {
+    const int j = j0 + (lane & 7);
+    int cj = -1, nj = 0;
+    float sj = -INFINITY;
+    if (lane < 8 && j < r) {
+      cj = __ldcg(ids + j);
+      nj = __ldcg(cnts + j);
+      if (cj >= 0 && cj < a.C && nj > 0) sj = __ldcg(sc + cj) * kLog2e;
+      else nj = 0;
+    }
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int cu = __shfl_sync(kFull, cj, u);
+      v[u] = (cu >= 0 && cu < a.C) ? __ldg(vs + (size_t)cu * (kD / 4) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mt = sj;
+#pragma unroll
+    for (int o2 = 4; o2 > 0; o2 >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o2));
+    mt = __shfl_sync(kFull, mt, 0);
+    if (mt > -INFINITY) {
+      const float mn = fmaxf(m, mt);
+      const float corr = (m > -INFINITY) ? exp2f(m - mn) : 0.f;
+      const float p = (sj > -INFINITY) ? exp2f(sj - mn) : 0.f;
+      l *= corr;
+      o.x *= corr;
+      o.y *= corr;
+      o.z *= corr;
+      o.w *= corr;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float pu = __shfl_sync(kFull, p, u);
+        const float nu = (float)__shfl_sync(kFull, nj, u);
+        l += pu * nu;
+        o.x += pu * v[u].x;
+        o.y += pu * v[u].y;
+        o.z += pu * v[u].z;
+        o.w += pu * v[u].w;
+      }
+      m = mn;
+    }
+  }
+  combine_write(S, m, l, o, a.neg_part + (size_t)bh * kPartStride, -1.f);
+}
+
+// ---------------------------------------------------------------------------
+// merge of one query head (all 512 consumers)
+// ---------------------------------------------------------------------------
+// Partials: steady pieces, retrieved pieces (exact, +), the KV group's
+// estimate pieces (every non-empty cluster, +) and the selected clusters'
+// estimate (-).  out = O / L, lse = (M + log2 L) ln 2.  Every partial is
+// loaded in one round of independent loads (thread (q, d) holds element d of
+// the partials q, q + 4, ...), so the merge costs one global round trip.
+template <int G>
+__device__ void merge_head(const DecodeArgs& a, DecSmem& S, int bh) {
+  constexpr int kPerThread = 8;  // partials per thread and round: 32 per round
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / G, hl = h - g * G;
+  const int bg = b * a.Hkv + g;
+  const long long H = (long long)a.B * a.Hq;
+  // piece owners (a block with an empty range wrote no piece)
+  const long long nst = H * a.tph, nr = H * a.r;
+  int s_lo = 0, s_hi = -1, r_lo = 0, r_hi = -1;
+  if (a.tph > 0) {
+    s_lo = part_owner((long long)bh * a.tph, nst, a.nb);
+    s_hi = part_owner((long long)bh * a.tph + a.tph - 1, nst, a.nb);
+  }
+  if (a.r > 0) {
+    r_lo = part_owner((long long)bh * a.r, nr, a.nb);
+    r_hi = part_owner((long long)bh * a.r + a.r - 1, nr, a.nb);
+  }
+  // estimate pieces: the scoring blocks whose value-sum share meets the group
+  const int nk = a.nb - a.nsel;
+  const long long nt = (long long)a.B * a.Hkv * a.tpg;
+  const int e_lo = part_owner((long long)bg * a.tpg, nt, nk);
+  const int e_hi = part_owner((long long)bg * a.tpg + a.tpg - 1, nt, nk);
+  const int ns_ = s_hi - s_lo + 1, nr_ = r_hi - r_lo + 1, ne_ = e_hi - e_lo + 1;
+  const int P = ns_ + nr_ + ne_ + 1;
+  // pointer of partial i, or null when that block wrote none
+  // (with at least nb units every block owns some, and no division is needed)
+  auto part = [&](int i) -> const float* {
+    if (i < ns_) {
+      const int o = s_lo + i;
+      if (nst < a.nb && part_lo(o, nst, a.nb) == part_lo(o + 1, nst, a.nb)) return nullptr;
+      return a.std_part + (size_t)(o + bh) * kPartStride;
+    }
+    i -= ns_;
+    if (i < nr_) {
+      const int o = r_lo + i;
+      if (nr < a.nb && part_lo(o, nr, a.nb) == part_lo(o + 1, nr, a.nb)) return nullptr;
+      return a.ret_part + (size_t)(o + bh) * kPartStride;
+    }
+    i -= nr_;
+    if (i < ne_) {
+      const int o = e_lo + i;
+      if (nt < nk && part_lo(o, nt, nk) == part_lo(o + 1, nt, nk)) return nullptr;
+      return a.est_part + ((size_t)(a.nsel + o + bg) * G + hl) * kPartStride;
+    }
+    return a.neg_part + (size_t)bh * kPartStride;
+  };
+  // partial pointers, computed once (thread i: partial i)
+  const float** ptrs = reinterpret_cast<const float**>(S.u.w);     // [P]
+  float* wm = S.u.w + 2 * 1024;                                     // [32] m, then weight
+  float* wl = wm + 64;                                              // [32] l
+  for (int i = tid; i < P; i += kCT) ptrs[i] = part(i);
+  csync();
+  const int dim = tid & (kD - 1), qq = tid >> 7;
+  float M = -INFINITY, L = 0.f, O = 0.f;
+  for (int base = 0; base < P; base += 4 * kPerThread) {
+    const int np = min(4 * kPerThread, P - base);
+    // one round of independent loads: (m, l) by threads < np, element dim of
+    // partials base + qq + 4u by thread (qq, dim)
+    float mi = -INFINITY, li = 0.f;
+    if (tid < np) {
+      const float* p = ptrs[base + tid];
+      if (p) {
+        mi = __ldcg(p);
+        li = __ldcg(p + 1);
+      }
+    }
+    float ov[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int i = qq + 4 * u;
+      const float* p = i < np ? ptrs[base + i] : nullptr;
+      ov[u] = p ? __ldcg(p + 2 + dim) : 0.f;
+    }
+    // warp 0: new running max, weights of this round's partials, L
+    if (warp == 0) {
+      float mc = fmaxf(M, warp_max(mi));
+      const float f = (mi > -INFINITY) ? exp2f(mi - mc) : 0.f;
+      const float corr = (M > -INFINITY) ? exp2f(M - mc) : 0.f;
+      const float lr = warp_sum(f * li);
+      if (lane < 32) wm[lane] = f;
+      if (lane == 0) {
+        wl[0] = mc;
+        wl[1] = corr;
+        wl[2] = lr;
+      }
+    }
+    csync();
+    const float Mn = wl[0], corr = wl[1];
+    if (Mn > -INFINITY) {
+      L = L * corr + wl[2];
+      O *= corr;
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        const int i = qq + 4 * u;
+        if (i < np) O += wm[i] * ov[u];
+      }
+      M = Mn;
+    }
+    csync();
+  }
+  float* red = &S.red_o[0][0];
+  if (qq > 0) red[(qq - 1) * kD + dim] = O;
+  csync();
+  if (qq == 0) {
+    O += red[dim] + red[kD + dim] + red[2 * kD + dim];
+    a.out[(size_t)bh * kD + dim] = (L > 0.f) ? O / L : 0.f;
+    if (a.lse != nullptr && dim == 0) a.lse[bh] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+  csync();
+}
+
+// ---------------------------------------------------------------------------
+// producer warp
+// ---------------------------------------------------------------------------
+template <int G>
+__device__ void producer(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
+  const int lane = threadIdx.x & 31;
+  uint32_t seq = 0;
+  // test hook: the first tile with copies in every block loses them
+  bool inject = a.inject != 0, skipped = false;
+  const int ns = a.sink + a.window;
+
+  // claim the next ring slot (warp-uniform); false once this block aborted
+  auto slot = [&](int& stage) -> bool {
+    stage = (int)(seq % kStages);
+    int good = 1;
+    if (lane == 0) {
+      if (*(volatile int*)&S.abort) {
+        good = 0;
+      } else if (seq >= (uint32_t)kStages) {
+        good = mbar_wait(smem_addr(&S.empty[stage]), ((seq / kStages) - 1u) & 1u, a.status);
+      }
+      if (good) fence_proxy_async_smem();
+      else S.abort = 1;
+    }
+    return __shfl_sync(kFull, good, 0) != 0;
+  };
+  // lane 0: tile description + expected bytes; then lanes issue the copies
+  auto post = [&](int stage, int kind, int bh, int ntok, int last, int units, uint32_t bytes) {
+    if (lane == 0) {
+      TileInfo t;
+      t.kind = kind;
+      t.bh = bh;
+      t.ntok = ntok;
+      t.last = last;
+      t.units = units;
+      t.pad0 = t.pad1 = t.pad2 = 0;
+      S.info[stage] = t;
+      mbar_arrive_expect_tx(smem_addr(&S.full[stage]), bytes);
+    }
+    __syncwarp();
+  };
+  auto commit = [&]() {
+    if (__any_sync(kFull, skipped)) inject = false;
+    __syncwarp();
+    if (lane == 0) S.issued = (int)(seq + 1);
+    ++seq;
+  };
+  auto copy = [&](int stage, uint32_t dst_off, const void* src, uint32_t bytes) {
+    if (inject) skipped = true;
+    else bulk_g2s(smem_addr(S.ring[stage]) + dst_off, src, bytes, smem_addr(&S.full[stage]));
+  };
+  auto copy_q = [&](int stage, const void* src, uint32_t bytes) {
+    if (inject) skipped = true;
+    else bulk_g2s(smem_addr(S.qs[stage]), src, bytes, smem_addr(&S.full[stage]));
+  };
+
+  // stages 1 and 2 (scoring blocks): centroid-key tiles kj, kj + nk, ...;
+  // then the value-sum tiles [v0, v1)
+  for (int pass = 0; pass < 2; ++pass) {
+    if (sc.sel || !(a.stages & (pass == 0 ? kStageScore : kStageSelect))) continue;
+    const float* src = pass == 0 ? a.kbar : a.vsum;
+    const int n = pass == 0 ? sc.n1 : sc.v1 - sc.v0;
+    for (int i = 0; i < n; ++i) {
+      const int T = pass == 0 ? sc.kj + i * sc.nk : sc.v0 + i;
+      int stage;
+      if (!slot(stage)) return;
+      const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
+      const int nrows = min(kTile, a.C - c0);
+      const uint32_t qbytes = pass == 0 ? (uint32_t)G * kD * 2 : 0u;
+      post(stage, kTileIndex, bg, nrows, 0, 0, (uint32_t)nrows * 512u + qbytes);
+      if (lane == 0) copy(stage, 0, src + ((size_t)bg * a.C + c0) * kD, (uint32_t)nrows * 512u);
+      if (lane == 1 && pass == 0) {
+        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+        copy_q(stage, a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD, qbytes);
+      }
+      commit();
+    }
+  }
+  if (!(a.stages & kStageAttend)) return;
+
+  // stage 3a: steady tiles
+  for (long long T = sc.s0; T < sc.s1; ++T) {
+    int stage;
+    if (!slot(stage)) return;
+    const int bh = (int)(T / a.tph), j = (int)(T - (long long)bh * a.tph);
+    const int u0 = j * kTile, u1 = min(ns, u0 + kTile), n = u1 - u0;
+    const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+    const size_t head = (size_t)b * a.Hkv + g;
+    const bool last = (j == a.tph - 1) || (T == sc.s1 - 1);
+    // units: steady tiles of this head inside the block's range
+    const long long first = max(sc.s0, (long long)bh * a.tph);
+    post(stage, kTileSteady, bh, n, last, last ? (int)(T - first + 1) : 0,
+         (uint32_t)n * 512u + kD * 2u);
+    // rows: [u0, min(u1, sink)) are positions u; the rest are N - window + (u - sink)
+    const int a1 = min(u1, a.sink);
+    if (lane < 2 && u0 < a1) {
+      const uint16_t* base = (lane == 0 ? a.K : a.V) + (head * a.N + u0) * kD;
+      copy(stage, lane == 0 ? 0u : kStageBytes / 2, base, (uint32_t)(a1 - u0) * 256u);
+    }
+    const int b0 = max(u0, a.sink);
+    if (lane >= 2 && lane < 4 && b0 < u1) {
+      const int row = a.N - a.window + (b0 - a.sink);
+      const uint16_t* base = (lane == 2 ? a.K : a.V) + (head * a.N + row) * kD;
+      const uint32_t dst = (uint32_t)(b0 - u0) * 256u + (lane == 2 ? 0u : kStageBytes / 2);
+      copy(stage, dst, base, (uint32_t)(u1 - b0) * 256u);
+    }
+    if (lane == 4) copy_q(stage, a.q + (size_t)bh * kD, kD * 2);
+    commit();
+  }
+
+  // stage 3b: retrieved tiles, each head's once its selection is published
+  if (sc.r0 < sc.r1) {
+    const int r = a.r, rs = r > 0 ? r : 1;
+    long long slot0 = sc.r0;
+    while (slot0 < sc.r1) {
+      const int bh = (int)(slot0 / r);
+      const int j_lo = (int)(slot0 - (long long)bh * r);
+      const int j_hi = (int)min((long long)r, sc.r1 - (long long)bh * r);
+      slot0 = (long long)bh * r + j_hi;
+      if (a.fused) {
+        int good = 1;
+        if (lane == 0) {
+          good = !*(volatile int*)&S.abort && count_wait(a.sel_ready + bh, 1u, a.status, &S.abort);
+          if (!good) S.abort = 1;
+        }
+        if (!__shfl_sync(kFull, good, 0)) return;
+        __syncwarp();  // the other lanes' loads come after lane 0's acquire
+      }
+      const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+      const size_t head = (size_t)b * a.Hkv + g;
+      const uint16_t* Ks = a.ksorted + head * (size_t)a.N_idx * kD;
+      const uint16_t* Vs = a.vsorted + head * (size_t)a.N_idx * kD;
+      const int* rows_g = a.sel_rows + (size_t)bh * rs;
+      const int* cnts_g = a.sel_cnts + (size_t)bh * rs;
+      // two windows of 32 clusters in registers: (row, count, piece-relative start)
+      auto load_win = [&](int j, int& row, int& cnt) {
+        row = 0;
+        cnt = 0;
+        if (j < j_hi) {
+          row = __ldcg(rows_g + j);
+          cnt = __ldcg(cnts_g + j);
+          if (cnt < 0 || row < 0 || (long long)row + cnt > a.N_idx) {
+            report(a.status, WI_ERR_INDEX_MISMATCH);
+            cnt = 0;
+            row = 0;
+          }
+        }
+      };
+      int rowA, cntA, rowB, cntB;
+      load_win(j_lo + lane, rowA, cntA);
+      load_win(j_lo + 32 + lane, rowB, cntB);
+      // exclusive prefix of counts over a window + its total
+      auto wscan = [&](int cnt, int& total) {
+        int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int t = __shfl_up_sync(kFull, incl, o);
           if (lane >= o) incl += t;
         }
-        const int excl = incl - tot;
-        if (excl < remaining && remaining <= incl) {
-          int acc = excl;
+        total = __shfl_sync(kFull, incl, 31);
+        return incl - cnt;
+      };
+      // window A = slots [jA, jA + 32), window B = the next 32; starts are
+      // piece-relative token positions
+      int jA = j_lo, totA, totB;
+      int stA = wscan(cntA, totA);
+      int stB = totA + wscan(cntB, totB);
+      int baseA = 0, cur = 0;
+      bool posted_last = false;
+      for (;;) {
+        const int avail = baseA + totA + totB - cur;
+        const bool more = jA + 64 < j_hi;
+        if (avail > 0) {
+          const int n = min(kTile, avail);
+          const bool last = (n == avail) && !more;
+          int stage;
+          if (!slot(stage)) return;
+          post(stage, kTileRet, bh, n, last, last ? j_hi - j_lo : 0,
+               (uint32_t)n * 512u + kD * 2u);
+          const int t0 = cur, t1 = cur + n;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (acc + cnt[j] >= remaining) {
-              S.i[1] = 255 - 8 * lane - j;
-              S.i[2] = acc;
-              S.i[3] = cnt[j];
-              break;
+          for (int w2 = 0; w2 < 2; ++w2) {
+            const int ca = baseA + (w2 == 0 ? stA : stB), cnt = w2 == 0 ? cntA : cntB;
+            const int row = w2 == 0 ? rowA : rowB;
+            const int x0 = max(t0, ca), x1 = min(t1, ca + cnt);
+            if (x0 < x1) {
+              const size_t srow = (size_t)row + (x0 - ca);
+              const uint32_t d = (uint32_t)(x0 - t0) * 256u, nb = (uint32_t)(x1 - x0) * 256u;
+              copy(stage, d, Ks + srow * kD, nb);
+              copy(stage, kStageBytes / 2 + d, Vs + srow * kD, nb);
             }
-            acc += cnt[j];
           }
-        }
-      }
-      __syncthreads();
-      remaining -= S.i[2];
-      count = S.i[3];
-      prefix |= (uint32_t)S.i[1] << shift;
-      mask |= 0xffu << shift;
-      if (count == remaining) break;  // the whole boundary bin is selected
-    }
-  }
-  const bool any = r_eff > 0;
-  const bool tie_cut = any && remaining < count;  // equal full keys at the boundary
-  int c_cut = INT_MAX;
-  const int per = (C + kK2Threads - 1) / kK2Threads;
-  const int my0 = min(C, tid * per), my1 = min(C, my0 + per);
-  if (tie_cut) {
-    int ne = 0;
-    for (int c = my0; c < my1; ++c) ne += (key(c) == prefix);
-    int2 tot;
-    const int before = block_scan2(make_int2(ne, 0), S.scan, &tot).x;
-    if (before < remaining && remaining <= before + ne) {
-      int cnt = before;
-      for (int c = my0; c < my1; ++c) {
-        if (key(c) == prefix && ++cnt == remaining) {
-          S.i[4] = c;
+          if (lane == 0) copy_q(stage, a.q + (size_t)bh * kD, kD * 2);
+          commit();
+          cur = t1;
+          if (last) {
+            posted_last = true;
+            break;
+          }
+        } else if (!more) {
           break;
         }
+        // window A used up: B becomes A, the next 32 slots are loaded into B
+        if (cur >= baseA + totA && jA + 32 < j_hi) {
+          baseA += totA;
+          rowA = rowB;
+          cntA = cntB;
+          stA = stB - totA;
+          totA = totB;
+          jA += 32;
+          load_win(jA + 32 + lane, rowB, cntB);
+          stB = totA + wscan(cntB, totB);
+        }
+      }
+      if (!posted_last) {  // the piece's slots must be reported even without tokens
+        int stage;
+        if (!slot(stage)) return;
+        post(stage, kTileRet, bh, 0, 1, j_hi - j_lo, 0u);
+        commit();
       }
     }
-    __syncthreads();
-    c_cut = S.i[4];
   }
-  auto is_sel = [&](uint32_t k, int c) {
-    return any && k != 0u &&
-           ((k & mask) > prefix || ((k & mask) == prefix && (!tie_cut || c <= c_cut)));
-  };
-  // ordered compaction: ids ascending, exclusive prefix of member counts
-  int nsel = 0, ntok = 0;
-  for (int c = my0; c < my1; ++c) {
-    if (is_sel(key(c), c)) {
-      ++nsel;
-      ntok += __ldg(sz + c);
-    }
-  }
-  int2 total;
-  const int2 ex = block_scan2(make_int2(nsel, ntok), S.scan, &total);
-  int* ids = a.sel_ids + (size_t)bh * r;
-  int* pre = a.sel_prefix + (size_t)bh * (r + 1);
-  int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
-  int pos = ex.x, tok = ex.y;
-  for (int c = my0; c < my1; ++c) {
-    if (is_sel(key(c), c)) {
-      ids[pos] = c;
-      pre[pos] = tok;
-      if (topk) topk[pos] = c;
-      ++pos;
-      tok += __ldg(sz + c);
-    }
-  }
-  for (int i = total.x + tid; i <= r; i += kK2Threads) {
-    pre[i] = total.y;
-    if (i < r) {
-      ids[i] = -1;
-      if (topk) topk[i] = -1;
-    }
-  }
+  // end marker
+  int stage;
+  if (!slot(stage)) return;
+  post(stage, kTileEnd, 0, 0, 0, 0, 0u);
+  commit();
 }
 
-// Role (b): estimate of every non-empty cluster of a 256-cluster chunk of one
-// KV head, for each of its G query heads.  Warp w takes 16 consecutive
-// clusters: lane i < 16 computes e^{s - m_warp} for cluster i (m_warp = the
-// warp's max score), then the 16 value-sum rows are streamed with 128-bit
-// loads and accumulated with the broadcast weights.
+// ---------------------------------------------------------------------------
+// consumer tiles
+// ---------------------------------------------------------------------------
+// Consumers copy their share of a staged tile into registers and release the
+// stage at once, so that the ring refills while they compute.  Per-row side
+// data (cluster sizes; scores in stage 2) is fetched kSideAhead tiles ahead with
+// cp.async into per-warp slots: lane 0 holds the sizes of the warp's 4 rows,
+// lane h < G the scores of head h.  (Plain loads in flight would be waited
+// for by every warp barrier on the way.)
+
+// Centroid-key tile: warp w scores rows 4w..4w+3 for the G heads of the group.
 template <int G>
-__device__ void estimate_all(const DecodeArgs& a, int bg, int chunk, float* red) {
-  float(*red_o)[G][kD] = reinterpret_cast<float(*)[G][kD]>(red);
-  float* red_m = red + kK2Warps * G * kD;
-  float* red_l = red_m + kK2Warps * G;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-  const int c_end = min(a.C, (chunk + 1) * kEstChunk);
-  const int base = chunk * kEstChunk + warp * kEstBatch;
-  const int c = base + (lane & 15);
-  const bool valid = c < c_end;
-  const int n = valid ? __ldg(a.size + (size_t)bg * a.C + c) : 0;
-  float p[G], mw[G], lw[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const size_t bh = (size_t)b * a.Hq + g * G + h;
-    const float s = (n > 0) ? __ldcg(a.scores + bh * a.C + c) * kLog2e : -INFINITY;
-    float m = s;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    mw[h] = m;
-    p[h] = (s > -INFINITY) ? exp2f(s - m) : 0.f;
-    lw[h] = lane < 16 ? p[h] * (float)n : 0.f;
-  }
-  const float4* vs = reinterpret_cast<const float4*>(a.vsum + ((size_t)bg * a.C) * kD);
-  float4 v[kEstBatch];
-#pragma unroll
-  for (int j = 0; j < kEstBatch; ++j)
-    v[j] = (base + j < c_end) ? __ldg(vs + (size_t)(base + j) * (kD / 4) + lane)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-    for (int j = 0; j < kEstBatch; ++j) {
-      const float pj = __shfl_sync(kFull, p[h], j);
-      acc0 += pj * v[j].x;
-      acc1 += pj * v[j].y;
-      acc2 += pj * v[j].z;
-      acc3 += pj * v[j].w;
-    }
-    lw[h] = warp_sum(lw[h]);
-    reinterpret_cast<float4*>(red_o[warp][h])[lane] = make_float4(acc0, acc1, acc2, acc3);
-    if (lane == 0) {
-      red_m[warp * G + h] = mw[h];
-      red_l[warp * G + h] = lw[h];
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < G * kD; idx += kK2Threads) {
-    const int h = idx / kD, dim = idx - h * kD;
-    float M = -INFINITY;
-    for (int w = 0; w < kK2Warps; ++w) M = fmaxf(M, red_m[w * G + h]);
-    float L = 0.f, O = 0.f;
-    if (M > -INFINITY) {
-      for (int w = 0; w < kK2Warps; ++w) {
-        const float mwh = red_m[w * G + h];
-        const float f = mwh > -INFINITY ? exp2f(mwh - M) : 0.f;
-        L += red_l[w * G + h] * f;
-        O += red_o[w][h][dim] * f;
-      }
-    }
-    const size_t bh = (size_t)b * a.Hq + g * G + h;
-    float* P = a.est_part + (bh * a.est_chunks + chunk) * kPartStride;
-    if (dim == 0) {
-      P[0] = (L > 0.f) ? M : -INFINITY;
-      P[1] = L;
-    }
-    P[2 + dim] = O;
-  }
-}
-
-template <int G>
-__global__ void __launch_bounds__(kK2Threads) select_kernel(DecodeArgs a, int n_sel, int cached) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ SelShared S;
-  grid_dep_launch();
-  grid_dep_wait();
-  if ((int)blockIdx.x < n_sel) {
-    select_head(a, blockIdx.x, reinterpret_cast<uint32_t*>(smem), S, cached);
-  } else {
-    const int idx = blockIdx.x - n_sel;
-    const int bg = idx / a.est_chunks;
-    estimate_all<G>(a, bg, idx - bg * a.est_chunks, reinterpret_cast<float*>(smem));
-  }
-}
-
-// --------------------------------------------------------------------------
-// K3: exact attention + retrieved-estimate subtraction + merge
-// --------------------------------------------------------------------------
-constexpr int kAttThreads = 256;
-constexpr int kAttWarps = kAttThreads / 32;
-constexpr int kTile = 64;      // tokens per pipeline stage (8 per warp)
-constexpr int kStages = 2;
-constexpr int kWinCap = 512;   // retrieved clusters staged per window
-
-struct __align__(128) AttSmem {
-  uint16_t k[kStages][kTile * kD];  // bulk-copy destinations: 16-byte aligned
-  uint16_t v[kStages][kTile * kD];
-  float red_o[2][kAttWarps][kD];    // written as float4: 16-byte aligned
-  float red_m[2][kAttWarps];
-  float red_l[2][kAttWarps];
-  unsigned long long bar[kStages];  // mbarriers: 8-byte aligned
-  int win_prefix[kWinCap + 1];
-  int win_row[kWinCap];
-  int win_cid[kWinCap];
-  int last;
+struct KbarRegs {
+  float4 k[4];
+  uint2 q[G];
 };
-static_assert(offsetof(AttSmem, v) % 128 == 0, "staging buffer alignment");
-static_assert(offsetof(AttSmem, red_o) % 16 == 0, "float4 reduction buffer alignment");
-static_assert(offsetof(AttSmem, bar) % 8 == 0, "mbarrier alignment");
-// the merge reuses the staging buffers (K and V, all stages) for per-partial weights
-constexpr int kMergeMaxPartials = (int)(2 * sizeof(uint16_t) * kStages * kTile * kD / sizeof(float));
-
-__device__ void combine_warps(AttSmem& S, int slot, float m_run, float l_run, float o0, float o1,
-                              float o2, float o3, float sign, float* P, bool ok) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (lane == 0) {
-    S.red_m[slot][warp] = m_run;
-    S.red_l[slot][warp] = l_run;
+template <int G>
+__device__ __forceinline__ void kbar_load(const DecSmem& S, int stage, int nrows, KbarRegs<G>& t,
+                                          int lane, int warp) {
+  const float* kb = reinterpret_cast<const float*>(S.ring[stage]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = warp * 4 + j;
+    t.k[j] = row < nrows ? lds4(kb + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  reinterpret_cast<float4*>(S.red_o[slot][warp])[lane] = make_float4(o0, o1, o2, o3);
-  __syncthreads();
-  if (tid < kD) {
-    float M = -INFINITY;
-    for (int w = 0; w < kAttWarps; ++w) M = fmaxf(M, S.red_m[slot][w]);
-    float L = 0.f, O = 0.f;
-    if (ok && M > -INFINITY) {
-      for (int w = 0; w < kAttWarps; ++w) {
-        const float mw = S.red_m[slot][w];
-        const float f = mw > -INFINITY ? exp2f(mw - M) : 0.f;
-        L += S.red_l[slot][w] * f;
-        O += S.red_o[slot][w][tid] * f;
-      }
-    } else {
-      M = -INFINITY;
-    }
-    if (tid == 0) {
-      P[0] = M;
-      P[1] = sign * L;
-    }
-    P[2 + tid] = sign * O;
+#pragma unroll
+  for (int h = 0; h < G; ++h) t.q[h] = lds2(S.qs[stage] + h * kD * 2 + lane * 8);
+}
+// Lane L < 4G gets the score of row 4w + L / G for head L mod G.
+template <int G>
+__device__ __forceinline__ float kbar_dot(const DecodeArgs& a, const KbarRegs<G>& t, int lane) {
+  float v[4 * G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float q0 = bf_lo(t.q[h].x) * a.scale, q1 = bf_hi(t.q[h].x) * a.scale;
+    const float q2 = bf_lo(t.q[h].y) * a.scale, q3 = bf_hi(t.q[h].y) * a.scale;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v[j * G + h] = t.k[j].x * q0 + t.k[j].y * q1 + t.k[j].z * q2 + t.k[j].w * q3;
+  }
+  return reduce_scatter<4 * G>(v, lane);
+}
+template <int G>
+__device__ __forceinline__ void kbar_store(const DecodeArgs& a, float tot, int T, int4 n4,
+                                           int lane, int warp) {
+  const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
+  const int nrows = min(kTile, a.C - c0);
+  const int L = lane & (4 * G - 1), j = L / G, h = L - j * G;
+  const int nx = __shfl_sync(kFull, n4.x, 0), ny = __shfl_sync(kFull, n4.y, 0);
+  const int nz = __shfl_sync(kFull, n4.z, 0), nw = __shfl_sync(kFull, n4.w, 0);
+  const int n = j == 0 ? nx : (j == 1 ? ny : (j == 2 ? nz : nw));
+  const int row = warp * 4 + j;
+  if (lane < 4 * G && row < nrows) {
+    const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+    a.scores[((size_t)b * a.Hq + g * G + h) * a.C + c0 + row] = n > 0 ? tot : -INFINITY;
   }
 }
 
-__device__ void attend_tokens(const DecodeArgs& a, int bh, int sp, AttSmem& S) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / a.G;
-  const size_t head = (size_t)b * a.Hkv + g;
-  const uint16_t* Kh = a.K + head * (size_t)a.N * kD;
-  const uint16_t* Vh = a.V + head * (size_t)a.N * kD;
-  const uint16_t* Ksh = a.ksorted + head * (size_t)a.N_idx * kD;
-  const uint16_t* Vsh = a.vsorted + head * (size_t)a.N_idx * kD;
-  const float4* vsum = reinterpret_cast<const float4*>(a.vsum + head * (size_t)a.C * kD);
-  const float* sc = a.scores + (size_t)bh * a.C;
-  const int* off = a.offset + head * (size_t)(a.C + 1);
-  const int* ids = a.sel_ids + (size_t)bh * a.r;
-  const int* pre = a.sel_prefix + (size_t)bh * (a.r + 1);
-  const int ns = a.sink + a.window;
-  const int T_h = ns + pre[a.r];
-  const int lo = (int)((long long)T_h * sp / a.att_splits);
-  const int hi = (int)((long long)T_h * (sp + 1) / a.att_splits);
+// Per-warp estimate state for the G heads of one KV group.
+template <int G>
+struct EstState {
+  float m[G];      // running max (log2 units), warp-uniform
+  float4 o[G];     // this lane's 4 dimensions
+  float lacc;      // lane L < 4G: running sum n e^{s-m} for head L mod G
+};
 
-  const float qs = a.scale * kLog2e;
-  const uint2 qw = reinterpret_cast<const uint2*>(a.q + (size_t)bh * kD)[lane];
-  const float q0 = bf_lo(qw.x) * qs, q1 = bf_hi(qw.x) * qs;
-  const float q2 = bf_lo(qw.y) * qs, q3 = bf_hi(qw.y) * qs;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&S.bar[s]), 1);
-    fence_mbar_init();
+template <int G>
+__device__ __forceinline__ void est_reset(EstState<G>& e) {
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    e.m[h] = -INFINITY;
+    e.o[h] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  __syncthreads();
+  e.lacc = 0.f;
+}
 
-  float m_run = -INFINITY, l_run = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  // estimates of the retrieved clusters whose first token lies in this block
-  float m_neg = -INFINITY, l_neg = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
-  uint32_t phase = 0;
-  bool ok = true;
-  int round_lo = lo;
-  while (ok && round_lo < hi) {
-    int round_hi = hi;
-    int n_cl = 0;
-    if (hi > ns) {
-      // window of retrieved clusters overlapping [round_lo, hi)
-      const int lo_u = max(round_lo - ns, 0), hi_u = hi - ns;
-      int cnt_le = 0, cnt_lt = 0;
-      for (int base = 0; base < a.r; base += kAttThreads) {
-        const int j = base + tid;
-        const int p = (j < a.r) ? pre[j] : INT_MAX;
-        cnt_le += __syncthreads_count(p <= lo_u);
-        cnt_lt += __syncthreads_count(p < hi_u);
-      }
-      const int i0 = cnt_le - 1;
-      n_cl = cnt_lt - i0;
-      if (n_cl > kWinCap) {
-        n_cl = kWinCap;
-        round_hi = ns + pre[i0 + kWinCap];
-      }
-      for (int j = tid; j <= n_cl; j += kAttThreads) S.win_prefix[j] = pre[i0 + j];
-      for (int j = tid; j < n_cl; j += kAttThreads) {
-        const int c = ids[i0 + j];
-        S.win_cid[j] = c;
-        S.win_row[j] = off[c];
-      }
-      __syncthreads();
+__device__ __forceinline__ void vsum_load(const DecSmem& S, int stage, int nrows, float4 (&v)[4],
+                                          int lane, int warp) {
+  const float* vs = reinterpret_cast<const float*>(S.ring[stage]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = warp * 4 + j;
+    v[j] = row < nrows ? lds4(vs + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Value-sum tile: warp w accumulates rows 4w..4w+3.  Lane h < G holds s4, the
+// scores of head h for the 4 rows; lane 0 holds n4, their sizes.
+template <int G>
+__device__ __forceinline__ void vsum_compute(const DecodeArgs& a, const float4 (&v)[4], int T,
+                                             float4 s4, int4 n4, EstState<G>& e, int lane,
+                                             int warp) {
+  const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
+  const int nrows = min(kTile, a.C - c0);
+  const int L = lane & (4 * G - 1), j = L / G, hL = L - j * G;
+  const float sx = __shfl_sync(kFull, s4.x, hL), sy = __shfl_sync(kFull, s4.y, hL);
+  const float sz = __shfl_sync(kFull, s4.z, hL), sw = __shfl_sync(kFull, s4.w, hL);
+  const float sj = j == 0 ? sx : (j == 1 ? sy : (j == 2 ? sz : sw));
+  const int nx = __shfl_sync(kFull, n4.x, 0), ny = __shfl_sync(kFull, n4.y, 0);
+  const int nz = __shfl_sync(kFull, n4.z, 0), nw = __shfl_sync(kFull, n4.w, 0);
+  const int n = j == 0 ? nx : (j == 1 ? ny : (j == 2 ? nz : nw));
+  const int row = warp * 4 + j;
+  const float x = (lane < 4 * G && row < nrows && n > 0 && sj > -INFINITY) ? sj * kLog2e
+                                                                            : -INFINITY;
+  float mt = x;
+#pragma unroll
+  for (int o = G; o < 4 * G; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
+  float mL = -INFINITY, corrL = 1.f;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float th = __shfl_sync(kFull, mt, h);
+    if (th > e.m[h]) {
+      const float corr = (e.m[h] > -INFINITY) ? exp2f(e.m[h] - th) : 0.f;
+      e.o[h].x *= corr;
+      e.o[h].y *= corr;
+      e.o[h].z *= corr;
+      e.o[h].w *= corr;
+      if (hL == h) corrL = corr;
+      e.m[h] = th;
     }
-    const int ntiles = (round_hi - round_lo + kTile - 1) / kTile;
-    int ci = 0;  // producer's cursor into the window
-    auto issue = [&](int t, int stage) {
-      const int t0 = round_lo + t * kTile;
-      const int t1 = min(t0 + kTile, round_hi);
-      const uint32_t bar = smem_addr(&S.bar[stage]);
-      mbar_arrive_expect_tx(bar, (uint32_t)(t1 - t0) * (2u * kD * 2u));
-      const uint32_t dk = smem_addr(S.k[stage]), dv = smem_addr(S.v[stage]);
-      uint32_t drow = 0;
-      for (int tt = t0; tt < t1;) {
-        const uint16_t *ks, *vs;
-        int cnt;
-        if (tt < a.sink) {
-          cnt = min(t1, a.sink) - tt;
-          ks = Kh + (size_t)tt * kD;
-          vs = Vh + (size_t)tt * kD;
-        } else if (tt < ns) {
-          const int row = a.N - a.window + (tt - a.sink);
-          cnt = min(t1, ns) - tt;
-          ks = Kh + (size_t)row * kD;
-          vs = Vh + (size_t)row * kD;
+    if (hL == h) mL = e.m[h];
+  }
+  e.lacc *= corrL;
+  const float p = (x > -INFINITY) ? exp2f(x - mL) : 0.f;
+  e.lacc += p * (float)n;
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float pj = __shfl_sync(kFull, p, jj * G + h);
+      e.o[h].x += pj * v[jj].x;
+      e.o[h].y += pj * v[jj].y;
+      e.o[h].z += pj * v[jj].z;
+      e.o[h].w += pj * v[jj].w;
+    }
+  }
+}
+
+// Writes the block's estimate piece of group bg (ntiles of its tiles) and
+// counts the tiles on the group's counter.
+template <int G>
+__device__ void est_flush(const DecodeArgs& a, DecSmem& S, EstState<G>& e, int bg, int ntiles,
+                          int lane) {
+  const int L = lane & (4 * G - 1);
+  const int hL = L % G;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float lh = warp_sum((lane < 4 * G && hL == h) ? e.lacc : 0.f);
+    float* dst = a.est_part + ((size_t)(blockIdx.x + bg) * G + h) * kPartStride;
+    combine_write(S, e.m[h], lh, e.o[h], dst, 1.f);
+  }
+  if (threadIdx.x == 0) atomicAdd(a.est_cnt + bg, (unsigned)ntiles);
+  est_reset(e);
+}
+
+// Exact-attention tile (steady or retrieved rows): warp w takes tokens
+// 4w..4w+3; online softmax in log2 units.
+struct AttState {
+  float m, l;
+  float4 o;
+};
+struct AttRegs {
+  uint2 k[4], v[4], q;
+};
+
+__device__ __forceinline__ void att_load(const DecSmem& S, int stage, int ntok, AttRegs& t,
+                                         int lane, int warp) {
+  const uint16_t* kt = reinterpret_cast<const uint16_t*>(S.ring[stage]);
+  const uint16_t* vt = kt + kTile * kD;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int tk = warp * 4 + i;
+    t.k[i] = tk < ntok ? lds2(kt + tk * kD + lane * 4) : make_uint2(0u, 0u);
+    t.v[i] = tk < ntok ? lds2(vt + tk * kD + lane * 4) : make_uint2(0u, 0u);
+  }
+  t.q = lds2(S.qs[stage] + lane * 8);
+}
+
+__device__ __forceinline__ void att_compute(const DecodeArgs& a, const AttRegs& t, int ntok,
+                                            AttState& st, int lane, int warp) {
+  if (warp * kRowsPerWarp >= ntok) return;
+  const float qs = a.scale * kLog2e;
+  const float q0 = bf_lo(t.q.x) * qs, q1 = bf_hi(t.q.x) * qs, q2 = bf_lo(t.q.y) * qs,
+              q3 = bf_hi(t.q.y) * qs;
+  float v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    v[i] = bf_lo(t.k[i].x) * q0 + bf_hi(t.k[i].x) * q1 + bf_lo(t.k[i].y) * q2 +
+           bf_hi(t.k[i].y) * q3;
+  const float mine = reduce_scatter<4>(v, lane);
+  float lg[4];
+  float mt = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    lg[i] = __shfl_sync(kFull, mine, i);
+    if (warp * 4 + i >= ntok) lg[i] = -INFINITY;
+    mt = fmaxf(mt, lg[i]);
+  }
+  const float mn = fmaxf(st.m, mt);
+  const float corr = (st.m > -INFINITY) ? exp2f(st.m - mn) : 0.f;
+  st.l *= corr;
+  st.o.x *= corr;
+  st.o.y *= corr;
+  st.o.z *= corr;
+  st.o.w *= corr;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (warp * 4 + i < ntok) {
+      const float p = exp2f(lg[i] - mn);
+      st.l += p;
+      st.o.x += p * bf_lo(t.v[i].x);
+      st.o.y += p * bf_hi(t.v[i].x);
+      st.o.z += p * bf_lo(t.v[i].y);
+      st.o.w += p * bf_hi(t.v[i].y);
+    }
+  }
+  st.m = mn;
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps
+// ---------------------------------------------------------------------------
+template <int G>
+__device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t seq = 0;
+  bool bad = false;  // uniform over the consumers
+  const long long H = (long long)a.B * a.Hq;
+  const unsigned grp_target = (unsigned)(a.tpg * kCW);  // (tile, warp) pairs of a group
+
+  // wait for the next tile; collective: every consumer gets the same answer
+  auto acquire = [&](int& stage) -> bool {
+    stage = (int)(seq % kStages);
+    int ok = 1;
+    if (tid == 0) {
+      ok = !*(volatile int*)&S.abort &&
+           mbar_wait(smem_addr(&S.full[stage]), (seq / kStages) & 1u, a.status);
+      if (ok) S.confirmed = (int)(seq + 1);
+      else S.abort = 1;
+    }
+    bad = cany(!ok);
+    return !bad;
+  };
+  // release a stage whose data this warp has copied to registers
+  auto release = [&](int stage) {
+    __syncwarp();
+    if (lane == 31) mbar_arrive(smem_addr(&S.empty[stage]));
+    ++seq;
+  };
+  // collective bounded wait until *cnt >= target (one launch running every
+  // stage; stage-only launches find their inputs complete)
+  auto wait_count = [&](const unsigned* cnt, unsigned target) -> bool {
+    if (!a.fused) return !bad;
+    int ok = 1;
+    if (tid == 0) {
+      ok = !*(volatile int*)&S.abort && count_wait(cnt, target, a.status, &S.abort);
+      if (!ok) S.abort = 1;
+    }
+    bad = cany(!ok) || bad;
+    return !bad;
+  };
+  // Every warp's scores of the previous tile were stored before the barrier
+  // of this tile's acquire: thread 0 publishes them with one count per warp.
+  auto signal_scored = [&](int bg) {
+    if (tid == 0) {
+      fence_gpu();
+      atomicAdd(a.grp_cnt + bg, (unsigned)kCW);
+    }
+  };
+  // Side data of tile T (T < 0: none) for the warp's 4 rows into slot
+  // i mod kSideSlots, i = the tile's position in the block's sequence (lane 0:
+  // the sizes; lane h < G: the scores of head h, stage 2 only).  Elements past
+  // the end of a group read as size 0 / score -inf.  One commit group per tile.
+  auto issue_side = [&](int T, int i, bool scores) {
+    if (T >= 0) {
+      SideSlot& sl = S.side[warp][i % kSideSlots];
+      const int bg = T / a.tpg, c = (T - bg * a.tpg) * kTile + warp * 4;
+      if (lane == 0) {
+        const int* p = a.size + (size_t)bg * a.C + c;
+        if (c + 4 <= a.C && ((uintptr_t)p & 15u) == 0) {
+          cp_async16(sl.n, p);
         } else {
-          const int u = tt - ns;
-          while (S.win_prefix[ci + 1] <= u) ++ci;
-          const int row = S.win_row[ci] + (u - S.win_prefix[ci]);
-          cnt = min(t1 - tt, S.win_prefix[ci + 1] - u);
-          if (row < 0 || row + cnt > a.N_idx) {
-            // inconsistent index (offset/size beyond the sorted arrays): report
-            // it and stage steady row 0 instead, keeping the byte count
-            report(a.status, WI_ERR_INDEX_MISMATCH);
-            for (int e = 0; e < cnt; ++e) {
-              bulk_g2s(dk + (drow + e) * (kD * 2), Kh, kD * 2, bar);
-              bulk_g2s(dv + (drow + e) * (kD * 2), Vh, kD * 2, bar);
-            }
-            tt += cnt;
-            drow += cnt;
-            continue;
+          for (int k = 0; k < 4; ++k) {
+            if (c + k < a.C) cp_async4(sl.n + k, p + k);
+            else sl.n[k] = 0;
           }
-          ks = Ksh + (size_t)row * kD;
-          vs = Vsh + (size_t)row * kD;
         }
-        bulk_g2s(dk + drow * (kD * 2), ks, (uint32_t)cnt * (kD * 2), bar);
-        bulk_g2s(dv + drow * (kD * 2), vs, (uint32_t)cnt * (kD * 2), bar);
-        tt += cnt;
-        drow += cnt;
       }
-    };
-    const bool skip_first = a.inject != 0 && blockIdx.x == 0 && round_lo == lo;
-    if (tid == 0)
-      for (int t = 0; t < min(kStages, ntiles); ++t)
-        if (!(skip_first && t == 0)) issue(t, t);
-
-    // while the first copies are in flight: the estimates to subtract, one
-    // warp per cluster (clusters that start inside this round)
-    for (int j = warp; j < n_cl; j += kAttWarps) {
-      const int start = ns + S.win_prefix[j];
-      if (start < round_lo || start >= round_hi) continue;
-      const int c = S.win_cid[j];
-      const float s = __ldcg(sc + c) * kLog2e;
-      const float n = (float)(S.win_prefix[j + 1] - S.win_prefix[j]);
-      const float4 vv = __ldg(vsum + (size_t)c * (kD / 4) + lane);
-      const float m_new = fmaxf(m_neg, s);
-      const float corr = exp2f(m_neg - m_new);
-      const float p = exp2f(s - m_new);
-      l_neg = l_neg * corr + p * n;
-      n0 = n0 * corr + p * vv.x;
-      n1 = n1 * corr + p * vv.y;
-      n2 = n2 * corr + p * vv.z;
-      n3 = n3 * corr + p * vv.w;
-      m_neg = m_new;
-    }
-
-    for (int t = 0; t < ntiles; ++t) {
-      const int stage = t % kStages;
-      const int ntok = min(kTile, round_hi - (round_lo + t * kTile));
-      const bool waited = mbar_wait(smem_addr(&S.bar[stage]), (phase >> stage) & 1u, a.status);
-      phase ^= 1u << stage;
-      if (!__syncthreads_and(waited)) {
-        // give up: first let the copies already issued for later tiles land
-        for (int u = t + 1; u < min(ntiles, t + kStages); ++u) {
-          const int s2 = u % kStages;
-          mbar_wait(smem_addr(&S.bar[s2]), (phase >> s2) & 1u, a.status);
-          phase ^= 1u << s2;
+      if (scores && lane < G) {
+        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+        const float* p = a.scores + ((size_t)b * a.Hq + g * G + lane) * a.C + c;
+        if (c + 4 <= a.C && ((uintptr_t)p & 15u) == 0) {
+          cp_async16(sl.s[lane], p);
+        } else {
+          for (int k = 0; k < 4; ++k) {
+            if (c + k < a.C) cp_async4(sl.s[lane] + k, p + k);
+            else sl.s[lane][k] = -INFINITY;
+          }
         }
-        ok = false;
+      }
+    }
+    cp_async_commit();
+  };
+  // after cp_async_wait: lane 0 gets the sizes, lane h < G the scores of head h
+  auto side_sizes = [&](int i) -> int4 {
+    return lane == 0 ? *reinterpret_cast<const int4*>(S.side[warp][i % kSideSlots].n)
+                     : make_int4(0, 0, 0, 0);
+  };
+  auto side_scores = [&](int i) -> float4 {
+    return lane < G ? *reinterpret_cast<const float4*>(S.side[warp][i % kSideSlots].s[lane])
+                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  };
+
+  // ---- stage 1 (scoring blocks): scores
+  if ((a.stages & kStageScore) && !sc.sel) {
+    auto T1 = [&](int i) { return i < sc.n1 ? sc.kj + i * sc.nk : -1; };
+    for (int i = 0; i < kSideAhead; ++i) issue_side(T1(i), i, false);
+    int prev_bg = -1;  // group of the previous tile, published after this tile's barrier
+    for (int i = 0; i < sc.n1; ++i) {
+      const int T = sc.kj + i * sc.nk;
+      issue_side(T1(i + kSideAhead), i + kSideAhead, false);
+      int stage;
+      if (!acquire(stage)) break;
+      if (prev_bg >= 0) signal_scored(prev_bg);
+      KbarRegs<G> t;
+      const int c0 = (T % a.tpg) * kTile;
+      kbar_load<G>(S, stage, min(kTile, a.C - c0), t, lane, warp);
+      release(stage);
+      cp_async_wait<kSideAhead>();
+      const float tot = kbar_dot<G>(a, t, lane);
+      kbar_store<G>(a, tot, T, side_sizes(i), lane, warp);
+      prev_bg = T / a.tpg;
+    }
+    cp_async_wait<0>();
+    if (!bad && prev_bg >= 0) {
+      csync();
+      signal_scored(prev_bg);
+    }
+  }
+
+  // ---- stage 2: selections (selection blocks); estimate of every cluster
+  // (scoring blocks)
+  if ((a.stages & kStageSelect) && !bad) {
+    if (sc.sel) {
+      for (int bh = sc.sel0; bh < H; bh += sc.sel_step) {
+        const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+        if (!wait_count(a.grp_cnt + (size_t)b * a.Hkv + g, grp_target)) break;
+        select_head<G>(a, S, bh);
+        if (tid == 0) atomicExch(a.sel_ready + bh, 1u);
+      }
+      // the estimates of this block's selections, published per head
+      if (!bad) {
+        for (int bh = sc.sel0; bh < H; bh += sc.sel_step) {
+          estimate_selected<G>(a, S, bh);
+          if (tid == 0) atomicExch(a.neg_ready + bh, 1u);
+        }
+      }
+    } else if (sc.v0 < sc.v1) {
+      for (int bg = sc.v0 / a.tpg; bg <= (sc.v1 - 1) / a.tpg; ++bg)
+        if (!wait_count(a.grp_cnt + bg, grp_target)) break;
+      if (!bad) {
+        EstState<G> e;
+        est_reset(e);
+        int cur_bg = -1, cur_n = 0;
+        const int n2 = sc.v1 - sc.v0;
+        for (int i = 0; i < kSideAhead; ++i) issue_side(i < n2 ? sc.v0 + i : -1, i, true);
+        for (int i = 0; i < n2; ++i) {
+          const int T = sc.v0 + i;
+          issue_side(i + kSideAhead < n2 ? T + kSideAhead : -1, i + kSideAhead, true);
+          const int bg = T / a.tpg;
+          if (bg != cur_bg) {  // same tiles in every warp: a uniform barrier
+            if (cur_bg >= 0) est_flush<G>(a, S, e, cur_bg, cur_n, lane);
+            cur_bg = bg;
+            cur_n = 0;
+          }
+          ++cur_n;
+          int stage;
+          if (!acquire(stage)) break;
+          float4 v[4];
+          const int c0 = (T % a.tpg) * kTile;
+          vsum_load(S, stage, min(kTile, a.C - c0), v, lane, warp);
+          release(stage);
+          cp_async_wait<kSideAhead>();
+          vsum_compute<G>(a, v, T, side_scores(i), side_sizes(i), e, lane, warp);
+        }
+        cp_async_wait<0>();
+        if (!bad && cur_bg >= 0) est_flush<G>(a, S, e, cur_bg, cur_n, lane);
+      }
+    }
+  }
+
+  // ---- stage 3: exact attention over steady and retrieved rows, merges
+  if ((a.stages & kStageAttend) && !bad) {
+    // a head merges once its group's estimate pieces and its negative estimate
+    // are written
+    auto merge_ready = [&](int bh) -> bool {
+      const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+      return wait_count(a.est_cnt + (size_t)b * a.Hkv + g, (unsigned)a.tpg) &&
+             wait_count(a.neg_ready + bh, 1u);
+    };
+    AttState st = {-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+    const int per_head = a.tph + a.r;
+    for (;;) {
+      int stage;
+      if (!acquire(stage)) break;
+      const TileInfo t = S.info[stage];
+      if (t.kind == kTileEnd) {
+        release(stage);
         break;
       }
-      const uint2* kt = reinterpret_cast<const uint2*>(S.k[stage]);
-      const uint2* vt = reinterpret_cast<const uint2*>(S.v[stage]);
-      constexpr int U = kTile / kAttWarps;  // tokens per warp per tile
-      float lg[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint2 kw = kt[(warp * U + u) * (kD / 4) + lane];
-        lg[u] = bf_lo(kw.x) * q0 + bf_hi(kw.x) * q1 + bf_lo(kw.y) * q2 + bf_hi(kw.y) * q3;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int u = 0; u < U; ++u) lg[u] += __shfl_xor_sync(kFull, lg[u], o);
-      float mt = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (warp * U + u >= ntok) lg[u] = -INFINITY;
-        mt = fmaxf(mt, lg[u]);
-      }
-      if (mt > -INFINITY) {
-        const float m_new = fmaxf(m_run, mt);
-        const float corr = exp2f(m_run - m_new);
-        l_run *= corr;
-        o0 *= corr;
-        o1 *= corr;
-        o2 *= corr;
-        o3 *= corr;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (warp * U + u < ntok) {
-            const float p = exp2f(lg[u] - m_new);
-            const uint2 vw = vt[(warp * U + u) * (kD / 4) + lane];
-            l_run += p;
-            o0 += p * bf_lo(vw.x);
-            o1 += p * bf_hi(vw.x);
-            o2 += p * bf_lo(vw.y);
-            o3 += p * bf_hi(vw.y);
-          }
+      AttRegs ar;
+      att_load(S, stage, t.ntok, ar, lane, warp);
+      release(stage);
+      att_compute(a, ar, t.ntok, st, lane, warp);
+      if (t.last) {
+        float* dst = (t.kind == kTileSteady ? a.std_part : a.ret_part) +
+                     (size_t)(blockIdx.x + t.bh) * kPartStride;
+        combine_write(S, st.m, st.l, st.o, dst, 1.f);
+        st.m = -INFINITY;
+        st.l = 0.f;
+        st.o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tid == 0) {
+          const unsigned old = atomicAdd(a.head_cnt + t.bh, (unsigned)t.units);
+          S.flag = (old + (unsigned)t.units == (unsigned)per_head);
+          if (S.flag) fence_gpu();  // the other pieces before this block's loads
         }
-        m_run = m_new;
-      }
-      __syncthreads();
-      if (tid == 0 && t + kStages < ntiles) {
-        fence_proxy_async_smem();
-        issue(t + kStages, stage);
+        csync();
+        if (S.flag) {
+          if (merge_ready(t.bh)) merge_head<G>(a, S, t.bh);
+          if (bad) break;
+        }
       }
     }
-    round_lo = round_hi;
-    __syncthreads();
+    // heads with no steady tile and no retrieval budget: one designated block
+    if (per_head == 0 && !bad) {
+      for (long long bh = blockIdx.x; bh < H && !bad; bh += a.nb)
+        if (merge_ready((int)bh)) merge_head<G>(a, S, (int)bh);
+    }
   }
-  float* P = a.att_part + ((size_t)bh * a.att_splits + sp) * 2 * kPartStride;
-  combine_warps(S, 0, m_run, l_run, o0, o1, o2, o3, 1.f, P, ok);
-  combine_warps(S, 1, m_neg, l_neg, n0, n1, n2, n3, -1.f, P + kPartStride, ok);
 }
 
-// Log-sum-exp merge of every partial of one query head: exact (+), retrieved
-// estimates (-) and estimation chunks (+).
-__device__ void merge_head(const DecodeArgs& a, int bh, AttSmem& S) {
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  DecSmem& S = *reinterpret_cast<DecSmem*>(smem_raw);
   const int tid = threadIdx.x;
-  float* w = reinterpret_cast<float*>(S.k);  // per-partial weight (reuses staging)
-  __shared__ float sh_red[kAttWarps];
-  const int n_att = 2 * a.att_splits;
-  const int P = n_att + a.est_chunks;
-  const float* PA = a.att_part + (size_t)bh * n_att * kPartStride;
-  const float* PE = a.est_part + (size_t)bh * a.est_chunks * kPartStride;
-  auto part = [&](int i) {
-    return i < n_att ? PA + (size_t)i * kPartStride : PE + (size_t)(i - n_att) * kPartStride;
-  };
-  float M = -INFINITY;
-  for (int i = tid; i < P; i += kAttThreads) {
-    const float m = __ldcg(part(i));
-    w[i] = m;
-    M = fmaxf(M, m);
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&S.full[s]), 1);
+      mbar_init(smem_addr(&S.empty[s]), kCW);
+    }
+    fence_mbar_init();
+    S.abort = 0;
+    S.issued = 0;
+    S.confirmed = 0;
+    S.flag = 0;
   }
-  M = warp_max(M);
-  if ((tid & 31) == 0) sh_red[tid >> 5] = M;
   __syncthreads();
-  M = -INFINITY;
-  for (int i = 0; i < kAttWarps; ++i) M = fmaxf(M, sh_red[i]);
+  const Sched sc = schedule(a, blockIdx.x);
+  if (tid >= kCT) producer<G>(a, S, sc);
+  else consumers<G>(a, S, sc);
   __syncthreads();
-  float L = 0.f;
-  for (int i = tid; i < P; i += kAttThreads) {
-    const float m = w[i];
-    const float f = (M > -INFINITY && m > -INFINITY) ? exp2f(m - M) : 0.f;
-    w[i] = f;
-    L += f * __ldcg(part(i) + 1);
+  if (tid == 0) {
+    // let every copy still in flight land before the block exits
+    for (int q = S.confirmed; q < S.issued; ++q)
+      mbar_wait(smem_addr(&S.full[q % kStages]), (uint32_t)(q / kStages) & 1u, a.status);
+    // the last block to finish clears the progress counters for the next launch
+    fence_gpu();
+    S.flag = atomicAdd(a.end_cnt, 1u) == (unsigned)(a.nb - 1);
+    if (S.flag) fence_gpu();
   }
-  L = warp_sum(L);
-  if ((tid & 31) == 0) sh_red[tid >> 5] = L;
   __syncthreads();
-  L = 0.f;
-  for (int i = 0; i < kAttWarps; ++i) L += sh_red[i];
-  // two threads per output dimension, each over half of the partials
-  const int dim = tid & (kD - 1), half = tid >> 7;
-  float O = 0.f;
-#pragma unroll 4
-  for (int i = half; i < P; i += 2) O += w[i] * __ldcg(part(i) + 2 + dim);
-  float* red = reinterpret_cast<float*>(S.red_o);
-  __syncthreads();
-  if (half == 1) red[dim] = O;
-  __syncthreads();
-  if (half == 0) {
-    O += red[dim];
-    a.out[(size_t)bh * kD + dim] = (L > 0.f) ? O / L : 0.f;
-    if (a.lse != nullptr && dim == 0) a.lse[bh] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+  if (S.flag) {
+    for (int i = tid; i < a.counter_words; i += kThreads) a.grp_cnt[i] = 0u;
+    if (tid == 0) *a.end_cnt = 0u;
   }
-}
-
-__global__ void __launch_bounds__(kAttThreads) attend_kernel(DecodeArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  AttSmem& S = *reinterpret_cast<AttSmem*>(smem);
-  grid_dep_launch();
-  grid_dep_wait();
-  const int bh = blockIdx.x / a.att_splits;
-  const int sp = blockIdx.x - bh * a.att_splits;
-  attend_tokens(a, bh, sp, S);
-  // the last block of this head to finish merges all of its partials
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) S.last = (atomicAdd(&a.counters[bh], 1) == a.att_splits - 1);
-  __syncthreads();
-  if (S.last) {
-    __threadfence();
-    merge_head(a, bh, S);
-    if (threadIdx.x == 0) a.counters[bh] = 0;  // ready for the next call
-  }
-}
-
-template <typename F>
-cudaError_t set_smem(F* f, size_t bytes) {
-  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 }  // namespace
 
-// --------------------------------------------------------------------------
-// launchers
-// --------------------------------------------------------------------------
-cudaError_t launch_decode_score(const DecodeArgs& a, cudaStream_t st) {
-  const int rows = 32 / a.G;
-  const int rows_per_sweep = kScoreWarps * (rows >= 16 ? rows : 2 * rows);
-  const long long target_blocks = 148LL * 4;
-  const long long rows_total = (long long)a.C * a.B * a.Hkv;
-  long long rpb = (rows_total + target_blocks - 1) / target_blocks;
-  rpb = ((rpb + rows_per_sweep - 1) / rows_per_sweep) * rows_per_sweep;
-  const int rows_per_block = (int)rpb;
-  const int blocks_per_head = (a.C + rows_per_block - 1) / rows_per_block;
-  const dim3 grid((unsigned)(blocks_per_head * a.B * a.Hkv));
-  switch (a.G) {
-    case 1: return launch_ex(score_kernel<1>, grid, dim3(kScoreThreads), 0, st, false, a, rows_per_block, blocks_per_head);
-    case 2: return launch_ex(score_kernel<2>, grid, dim3(kScoreThreads), 0, st, false, a, rows_per_block, blocks_per_head);
-    case 4: return launch_ex(score_kernel<4>, grid, dim3(kScoreThreads), 0, st, false, a, rows_per_block, blocks_per_head);
-    case 8: return launch_ex(score_kernel<8>, grid, dim3(kScoreThreads), 0, st, false, a, rows_per_block, blocks_per_head);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t decode_blocks(int* nb) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  *nb = sms < kMaxBlocks ? sms : kMaxBlocks;
+  return cudaSuccess;
 }
 
 template <int G>
-static cudaError_t launch_select_g(const DecodeArgs& a, cudaStream_t st) {
-  const int cached = a.C <= kSelCacheMax ? 1 : 0;
-  const size_t sel_smem = cached ? (size_t)a.C * sizeof(uint32_t) : 0;
-  const size_t est_smem = sizeof(float) * (size_t)kK2Warps * G * (kD + 2);
-  const size_t smem = sel_smem > est_smem ? sel_smem : est_smem;
+static cudaError_t launch_g(const DecodeArgs& a, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    const size_t mx = (size_t)kSelCacheMax * sizeof(uint32_t) > est_smem
-                          ? (size_t)kSelCacheMax * sizeof(uint32_t)
-                          : est_smem;
-    cudaError_t e = set_smem(select_kernel<G>, mx);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(DecSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int n_sel = a.B * a.Hq;
-  const int n_est = a.B * a.Hkv * a.est_chunks;
-  return launch_ex(select_kernel<G>, dim3((unsigned)(n_sel + n_est)), dim3(kK2Threads), smem, st,
-                   true, a, n_sel, cached);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.nb);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(DecSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<G>, a);
 }
 
-cudaError_t launch_decode_select(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   switch (a.G) {
-    case 1: return launch_select_g<1>(a, st);
-    case 2: return launch_select_g<2>(a, st);
-    case 4: return launch_select_g<4>(a, st);
-    case 8: return launch_select_g<8>(a, st);
+    case 1: return launch_g<1>(a, st);
+    case 2: return launch_g<2>(a, st);
+    case 4: return launch_g<4>(a, st);
+    case 8: return launch_g<8>(a, st);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_decode_attend(const DecodeArgs& a, cudaStream_t st) {
-  if (a.est_chunks + 2 * a.att_splits > kMergeMaxPartials) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = set_smem(attend_kernel, sizeof(AttSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return launch_ex(attend_kernel, dim3((unsigned)(a.B * a.Hq * a.att_splits)), dim3(kAttThreads),
-                   sizeof(AttSmem), st, true, a);
 }
 
 }  // namespace wi

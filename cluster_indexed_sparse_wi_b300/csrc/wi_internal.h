@@ -38,6 +38,16 @@ struct BuildArgs {
   }
 };
 
+// Most blocks one decode launch uses (one per SM); partial buffers are sized
+// for this many so that the workspace layout does not depend on the device.
+constexpr int kMaxBlocks = 256;
+constexpr int kPartStride = 2 + 128;  // (m, l, o[128]) per partial
+constexpr int kDecodeTile = 64;       // index rows / tokens per staging tile
+
+// Which decode stages one launch runs (wi_decode_attention runs all three,
+// with grid-wide barriers between them).
+enum : int { kStageScore = 1, kStageSelect = 2, kStageAttend = 4 };
+
 struct DecodeArgs {
   int B, Hq, Hkv, G, N, sink, window, r, C, N_idx;
   float scale;
@@ -52,28 +62,43 @@ struct DecodeArgs {
   const uint16_t* vsorted;
   // workspace regions
   int* status;
+  // per-launch progress counters, zero at the start of every launch (the last
+  // block to finish resets them)
+  unsigned* end_cnt;    // blocks finished
+  unsigned* grp_cnt;    // [B*Hkv] scored (index tile, warp) pairs of each KV group
+  unsigned* est_cnt;    // [B*Hkv] estimate pieces written for each KV group
+  unsigned* head_cnt;   // [B*Hq]  exact-attention units finished for each head
+  unsigned* sel_ready;  // [B*Hq]  1 once the head's selection is written
+  unsigned* neg_ready;  // [B*Hq]  1 once the estimate of its selection is written
+  int counter_words;    // words from grp_cnt to the end of neg_ready (contiguous)
   float* scores;        // [B,Hq,C]
   float* head_max;      // [B,Hq]
-  int* sel_ids;         // [B,Hq,r]   (r >= 1 slots)
-  int* sel_prefix;      // [B,Hq,r+1]
-  int* counters;        // [B,Hq]  arrival counters of the attention blocks
-  float* att_part;      // [B,Hq,att_splits,2,2+128]  (exact; minus retrieved estimate)
-  float* est_part;      // [B,Hq,est_chunks,2+128]
-  int att_splits, est_chunks, est_chunk_clusters;
-  int inject;           // test hook: block 0 skips its first staging copy
+  int* sel_ids;         // [B,Hq,rs]  retrieved ids ascending, -1 padding (rs = max(r,1))
+  int* sel_rows;        // [B,Hq,rs]  first sorted row of each retrieved cluster
+  int* sel_cnts;        // [B,Hq,rs]  members of each retrieved cluster (0 = padding)
+  float* est_part;      // [kMaxBlocks + B*Hkv][G][kPartStride]
+  float* std_part;      // [kMaxBlocks + B*Hq][kPartStride]
+  float* ret_part;      // [kMaxBlocks + B*Hq][kPartStride]
+  float* neg_part;      // [B*Hq][kPartStride]
+  // schedule (identical in every block)
+  int nb;               // grid size
+  int nsel;             // blocks [0, nsel) select; the others score
+  int stages;           // kStage* mask
+  int fused;            // the stages run in one launch and wait on each other
+  int tpg;              // index tiles per KV group: ceil(C / 64)
+  int tph;              // steady tiles per query head: ceil((sink + window) / 64)
+  int inject;           // test hook: every block skips the copies of its first tile
   // outputs
   int* topk_out;        // [B,Hq,r] or null
   float* out;           // [B,Hq,128]
   float* lse;           // [B,Hq] or null
 };
 
-constexpr int kPartStride = 2 + 128;  // (m, l, o[128]) per partial
-
-// decode launchers (wi_decode.cu)
-cudaError_t launch_decode_score(const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_decode_select(const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_decode_attend(const DecodeArgs& a, cudaStream_t st);
-constexpr int kEstChunk = 256;  // clusters per estimation block
+// decode launcher (wi_decode.cu): one persistent launch of the stages in
+// a.stages on a.nb blocks.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+// blocks a decode launch uses on the current device
+cudaError_t decode_blocks(int* nb);
 
 // build launchers (wi_build.cu)
 cudaError_t launch_build_init(const BuildArgs& a, cudaStream_t st);

@@ -53,11 +53,11 @@ extern "C" int wi_decode_attention_static(const wi_decode_params* p, const void*
   void* ws = nullptr;
   if ((st = scratch_address(&ws)) != WI_OK) return st;
   const cudaStream_t s = (cudaStream_t)stream;
-  // The scratch keeps the previous call's contents: the status word and the
-  // attention blocks' arrival counters must start at zero.
+  // The scratch keeps the previous call's contents: the status word, the grid
+  // barriers and the merge arrival counters must start at zero.
   char* base = static_cast<char*>(ws);
-  if (cudaMemsetAsync(base, 0, lay.scores, s) != cudaSuccess ||
-      cudaMemsetAsync(base + lay.counters, 0, lay.att_partials - lay.counters, s) != cudaSuccess)
+  if (cudaMemsetAsync(base, 0, lay.counters, s) != cudaSuccess ||
+      cudaMemsetAsync(base + lay.counters, 0, (size_t)lay.counter_bytes, s) != cudaSuccess)
     return WI_ERR_LAUNCH;
   return wi_decode_attention(p, q, K, V, index, out, lse, topk_ids, ws, kScratchBytes, stream);
 }

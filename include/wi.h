@@ -185,18 +185,24 @@ WI_API int wi_build_finalize(const wi_build_params *p, const void *K, const void
 WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_clusters);
 
 /* Byte offsets of the decode workspace regions (host struct), for
- * inspection of intermediate results.  No device work. */
+ * inspection of intermediate results.  No device work.  Partials are
+ * (m, l, o[d]) triples in log2 units (m is a log2-scaled logit). */
 typedef struct {
-  size_t scores;        /* f32 [B,Hq,C]    s_c = scale q.kbar_c, -inf if empty    */
-  size_t head_max;      /* f32 [B,Hq]      max_c s_c                             */
-  size_t selected;      /* i32 [B,Hq,r]    retrieved ids ascending, -1 padding    */
-  size_t sel_prefix;    /* i32 [B,Hq,r+1]  exclusive prefix of selected sizes     */
-  size_t counters;      /* i32 [B,Hq]      arrival counters (zero between calls)  */
-  size_t att_partials;  /* f32 [B,Hq,att_splits,2,2+d]  (m, l, o), log2 units:
-                           exact part, then minus the retrieved clusters' estimate */
-  size_t est_partials;  /* f32 [B,Hq,est_chunks,2+d]  estimate of every cluster   */
+  size_t counters;      /* grid-barrier words (256 B), then i32 [B,Hq] merge
+                           arrival counters and u32 [B,Hq] estimate-ready
+                           marks; zero before the first call, kept
+                           consistent by every call                          */
+  size_t scores;        /* f32 [B,Hq,C]   s_c = scale q.kbar_c, -inf if empty */
+  size_t head_max;      /* f32 [B,Hq]     max_c s_c                           */
+  size_t selected;      /* i32 [B,Hq,max(r,1)]  retrieved ids ascending, -1 pad */
+  size_t sel_rows;      /* i32 [B,Hq,max(r,1)]  first k_sorted row of each      */
+  size_t sel_counts;    /* i32 [B,Hq,max(r,1)]  its size n_c (0 for padding)     */
+  size_t partials;      /* f32 partials: estimate pieces, steady pieces,
+                           retrieved pieces, selected clusters' estimate       */
   size_t total;
-  int att_splits, est_chunks, est_chunk_clusters, reserved;
+  int counter_bytes;    /* bytes of the counters region                        */
+  int max_blocks;       /* blocks the partial buffers are sized for            */
+  int reserved0, reserved1;
 } wi_decode_layout;
 WI_API int wi_decode_workspace_layout(const wi_decode_params *p, int n_clusters,
                                wi_decode_layout *layout_out);
@@ -216,27 +222,30 @@ WI_API int wi_decode_workspace_layout(const wi_decode_params *p, int n_clusters,
  * f32; this reorders the arithmetic only.
  * q: bf16 [B,Hq,d]; out: f32 [B,Hq,d]; lse: f32 [B,Hq] or NULL;
  * topk_ids: i32 [B,Hq,r] (ascending ids, -1 padding) or NULL.
- * Equivalent to wi_decode_score, wi_decode_select, wi_decode_attend in order. */
+ * One persistent cooperative launch of one block per SM runs the three
+ * stages below with grid-wide barriers between them (the blocks must be
+ * co-resident: the launch fails with WI_ERR_LAUNCH otherwise).  Equivalent to
+ * wi_decode_score, wi_decode_select, wi_decode_attend in order. */
 WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const void *K, const void *V,
                         const wi_index *index, float *out, float *lse, int32_t *topk_ids,
                         void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 1: cluster scores s into the workspace (centroid-key scan). */
+/* Decode stage 1: cluster scores s into the workspace (a stream over the
+ * centroid keys). */
 WI_API int wi_decode_score(const wi_decode_params *p, const void *q, const wi_index *index,
                     void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 2, one launch with two roles: per query head, the retrieval
- * set T (radix select over the scores; ties to the lower id) with its token
- * prefix and the head's maximum score; and, per chunk of clusters, the
- * estimate of every non-empty cluster (log2-unit partials).  topk_ids may be
- * NULL. */
+/* Decode stage 2: per query head, the retrieval set T (radix select over the
+ * scores; ties to the lower id) with the clusters' sorted rows and sizes, the
+ * head's maximum score and the estimate of T (kept with a negative sign); and
+ * the estimate of every non-empty cluster (a stream over the value sums).
+ * topk_ids may be NULL. */
 WI_API int wi_decode_select(const wi_decode_params *p, const wi_index *index, int32_t *topk_ids,
                      void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
 /* Decode stage 3: exact attention over the steady zone and the retrieved
- * clusters (split over each head's token list), the retrieved clusters'
- * estimates with a negative sign, and the log-sum-exp merge of all partials
- * into out and lse (lse may be NULL). */
+ * clusters, and the log-sum-exp merge of every partial into out and lse (lse
+ * may be NULL). */
 WI_API int wi_decode_attend(const wi_decode_params *p, const void *q, const void *K, const void *V,
                      const wi_index *index, float *out, float *lse, void *workspace,
                      size_t workspace_bytes, wi_stream_t stream);
@@ -278,9 +287,9 @@ WI_API const char *wi_status_string(int status);
 
 /* Test hook for the device-side error path (no GPU fault involved): when bit 0
  * of `flags` is set, the next wi_decode_attention or wi_decode_attend call
- * makes its first exact-attention block skip its first staging copy.  That
- * block's bounded wait then runs out after about one second, the block
- * returns without output, and wi_sync_status reports WI_ERR_DEVICE_TIMEOUT.
+ * makes every block skip the copies of its first staging tile.  The blocks'
+ * bounded waits then run out after about one second, they return without
+ * output, and wi_sync_status reports WI_ERR_DEVICE_TIMEOUT.
  * The request is consumed by that one call.  Returns WI_OK. */
 WI_API int wi_debug_inject(int flags);
 

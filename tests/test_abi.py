@@ -119,11 +119,15 @@ def test_decode_layout(L):
     lay = L.DecodeLayout()
     assert lib.wi_decode_workspace_layout(ctypes.byref(dp(L)), 256, ctypes.byref(lay)) == 0
     assert lay.total == lib.wi_decode_workspace_bytes(ctypes.byref(dp(L)), 256)
-    regions = [lay.scores, lay.head_max, lay.selected, lay.sel_prefix, lay.counters,
-               lay.att_partials, lay.est_partials, lay.total]
+    regions = [lay.counters, lay.scores, lay.head_max, lay.selected, lay.sel_rows,
+               lay.sel_counts, lay.partials, lay.total]
     assert regions == sorted(regions) and all(r % 256 == 0 for r in regions)
     assert lay.head_max - lay.scores >= 8 * 256 * 4
-    assert lay.att_splits >= 1 and lay.est_chunks == 1
+    assert lay.scores - lay.counters == lay.counter_bytes >= 256 + 8 * 8
+    assert lay.sel_rows - lay.selected >= 8 * 8 * 4
+    # partial buffers: per block and KV group / query head, (m, l, o[128]) each
+    part = (2 + 128) * 4
+    assert lay.total - lay.partials >= part * ((lay.max_blocks + 2) * 4 + 2 * (lay.max_blocks + 8) + 8)
 
 
 @pytest.mark.parametrize("kw,code", [
