@@ -55,7 +55,7 @@ namespace {
 
 constexpr int kCW = 16;                       // consumer warps
 constexpr int kCT = kCW * 32;                 // consumer threads
-constexpr int kThreads = kCT + 32;            // + one producer warp
+constexpr int kThreads = kCT + 64;            // + one producer warp + one signaling warp
 constexpr int kStages = 4;
 constexpr int kTile = kDecodeTile;            // index rows or tokens per tile
 constexpr int kRowsPerWarp = kTile / kCW;     // 4
@@ -71,8 +71,17 @@ static_assert(kRowsPerWarp == 4, "tile layout");
 
 enum : int { kTileEnd = 0, kTileSteady = 1, kTileRet = 2, kTileIndex = 3 };
 
+// Written by the producer for every staged tile, so that the consumers do no
+// index arithmetic of their own.
 struct TileInfo {
-  int kind, bh, ntok, last, units, pad0, pad1, pad2;
+  int kind;
+  int bh;     // exact tiles: query head (b*Hq + h); index tiles: KV group (b*Hkv + g)
+  int ntok;   // rows (index tiles) or tokens (exact tiles) staged
+  int last;   // exact tiles: the piece ends with this tile
+  int units;  // exact tiles: units the piece adds to its head's arrival counter
+  int c0;     // index tiles: first cluster of the tile
+  int h0;     // index tiles: first query head of the group (b*Hq + g*G)
+  int pad;
 };
 
 struct Cand {
@@ -82,18 +91,16 @@ struct Cand {
   int row[kCand];
 };
 
-// Per-warp side data of one index tile (sizes of the warp's 4 rows; their
-// scores for each head of the group), fetched with cp.async kSideAhead tiles ahead.
-struct __align__(16) SideSlot {
-  int n[4];
-  float s[8][4];
+// Side data of one staged index tile: the sizes of its clusters and (value-sum
+// tiles) the scores of the group's query heads, staged with the tile.
+struct __align__(16) StageSide {
+  int n[kTile];
+  float s[8][kTile];
 };
-constexpr int kSideSlots = 8;  // prefetch distance kSideSlots - 2 tiles
-constexpr int kSideAhead = kSideSlots - 2;
 
 struct __align__(128) DecSmem {
   unsigned char ring[kStages][kStageBytes];  // bulk-copy destinations (16-byte aligned)
-  SideSlot side[kCW][kSideSlots];
+  StageSide sd[kStages];
   unsigned char qs[kStages][kQSlotBytes];
   float red_o[kCW][kD];
   float red_m[kCW];
@@ -115,8 +122,10 @@ struct __align__(128) DecSmem {
   int issued;             // tiles whose copies the producer issued
   int confirmed;          // tiles whose full barrier the consumers saw complete
   int flag;
+  int scored;             // stage-1 tiles whose scores every consumer warp has stored
 };
 static_assert(offsetof(DecSmem, qs) % 16 == 0, "bulk-copy alignment");
+static_assert(offsetof(DecSmem, sd) % 16 == 0, "bulk-copy alignment");
 static_assert(offsetof(DecSmem, red_o) % 16 == 0, "float4 alignment");
 static_assert(offsetof(DecSmem, full) % 8 == 0, "mbarrier alignment");
 static_assert(offsetof(DecSmem, u) % 16 == 0, "scratch union alignment");
@@ -145,18 +154,6 @@ __device__ __forceinline__ bool cany(bool x) {
 }
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ uint2 lds2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
-// Asynchronous global -> shared copies (cp.async): unlike plain loads, they
-// are not waited for by warp or block barriers, only by cp_async_wait.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 __device__ __forceinline__ uint32_t score_key(float s) {
   return (s == -INFINITY) ? 0u : float_key(s);  // 0 <=> empty cluster
 }
@@ -166,6 +163,14 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 // one thread adds to the count; a reader waits (acquire) until the count
 // reaches what it needs.
 __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -961,7 +966,8 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     return __shfl_sync(kFull, good, 0) != 0;
   };
   // lane 0: tile description + expected bytes; then lanes issue the copies
-  auto post = [&](int stage, int kind, int bh, int ntok, int last, int units, uint32_t bytes) {
+  auto post = [&](int stage, int kind, int bh, int ntok, int last, int units, uint32_t bytes,
+                  int c0 = 0, int h0 = 0) {
     if (lane == 0) {
       TileInfo t;
       t.kind = kind;
@@ -969,7 +975,9 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
       t.ntok = ntok;
       t.last = last;
       t.units = units;
-      t.pad0 = t.pad1 = t.pad2 = 0;
+      t.c0 = c0;
+      t.h0 = h0;
+      t.pad = 0;
       S.info[stage] = t;
       mbar_arrive_expect_tx(smem_addr(&S.full[stage]), bytes);
     }
@@ -989,26 +997,61 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     if (inject) skipped = true;
     else bulk_g2s(smem_addr(S.qs[stage]), src, bytes, smem_addr(&S.full[stage]));
   };
+  auto copy_to = [&](void* dst, const void* src, uint32_t bytes, int stage) {
+    if (inject) skipped = true;
+    else bulk_g2s(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]));
+  };
 
-  // stages 1 and 2 (scoring blocks): centroid-key tiles kj, kj + nk, ...;
-  // then the value-sum tiles [v0, v1)
+  // stages 1 and 2 (scoring blocks): centroid-key tiles kj, kj + nk, ...
+  // with the group's query rows and the clusters' sizes; then the value-sum
+  // tiles [v0, v1) with the sizes and the group's scores (each group's once
+  // every score of it is written)
+  const bool side_bulk = (a.C & 3) == 0;  // rows of sizes and scores start 16-byte aligned
   for (int pass = 0; pass < 2; ++pass) {
     if (sc.sel || !(a.stages & (pass == 0 ? kStageScore : kStageSelect))) continue;
     const float* src = pass == 0 ? a.kbar : a.vsum;
     const int n = pass == 0 ? sc.n1 : sc.v1 - sc.v0;
+    int ready_bg = -1;
     for (int i = 0; i < n; ++i) {
       const int T = pass == 0 ? sc.kj + i * sc.nk : sc.v0 + i;
-      int stage;
-      if (!slot(stage)) return;
       const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
       const int nrows = min(kTile, a.C - c0);
-      const uint32_t qbytes = pass == 0 ? (uint32_t)G * kD * 2 : 0u;
-      post(stage, kTileIndex, bg, nrows, 0, 0, (uint32_t)nrows * 512u + qbytes);
-      if (lane == 0) copy(stage, 0, src + ((size_t)bg * a.C + c0) * kD, (uint32_t)nrows * 512u);
-      if (lane == 1 && pass == 0) {
-        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-        copy_q(stage, a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD, qbytes);
+      const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+      const int h0 = b * a.Hq + g * G;
+      const float* srow = a.scores + (size_t)h0 * a.C + c0;  // scores[b, g*G, c0]
+      if (pass == 1 && bg != ready_bg && a.fused) {
+        int good = 1;
+        if (lane == 0) {
+          good = !*(volatile int*)&S.abort &&
+                 count_wait(a.grp_cnt + bg, (unsigned)(a.tpg * kCW), a.status, &S.abort);
+          if (good) fence_proxy_async_global();  // the scores, read by the copy engine
+          else S.abort = 1;
+        }
+        if (!__shfl_sync(kFull, good, 0)) return;
+        ready_bg = bg;
       }
+      int stage;
+      if (!slot(stage)) return;
+      const bool bulk = side_bulk && (nrows & 3) == 0;
+      const int nside = pass == 0 ? 1 : 1 + G;  // rows of side data (sizes, scores)
+      StageSide& sd = S.sd[stage];
+      if (!bulk) {  // ragged: plain loads, stored before the stage is posted
+        for (int k = lane; k < nside * kTile; k += 32) {
+          const int row = k / kTile, c = k - row * kTile;
+          if (row == 0) sd.n[c] = c < nrows ? __ldg(a.size + (size_t)bg * a.C + c0 + c) : 0;
+          else sd.s[row - 1][c] = c < nrows ? __ldcg(srow + (size_t)(row - 1) * a.C + c) : -INFINITY;
+        }
+        __syncwarp();
+      }
+      const uint32_t qbytes = pass == 0 ? (uint32_t)G * kD * 2 : 0u;
+      const uint32_t sbytes = bulk ? (uint32_t)(nside * nrows * 4) : 0u;
+      post(stage, kTileIndex, bg, nrows, 0, 0, (uint32_t)nrows * 512u + qbytes + sbytes, c0, h0);
+      if (lane == 0) copy(stage, 0, src + ((size_t)bg * a.C + c0) * kD, (uint32_t)nrows * 512u);
+      if (lane == 1 && pass == 0)
+        copy_q(stage, a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD, qbytes);
+      if (bulk && lane == 2) copy_to(sd.n, a.size + (size_t)bg * a.C + c0, (uint32_t)nrows * 4u, stage);
+      if (bulk && pass == 1 && lane >= 3 && lane < 3 + G)
+        copy_to(sd.s[lane - 3], srow + (size_t)(lane - 3) * a.C, (uint32_t)nrows * 4u, stage);
       commit();
     }
   }
@@ -1166,12 +1209,10 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
 // ---------------------------------------------------------------------------
 // consumer tiles
 // ---------------------------------------------------------------------------
-// Consumers copy their share of a staged tile into registers and release the
-// stage at once, so that the ring refills while they compute.  Per-row side
-// data (cluster sizes; scores in stage 2) is fetched kSideAhead tiles ahead with
-// cp.async into per-warp slots: lane 0 holds the sizes of the warp's 4 rows,
-// lane h < G the scores of head h.  (Plain loads in flight would be waited
-// for by every warp barrier on the way.)
+// Consumers copy their share of a staged tile (rows, query rows, side data)
+// into registers and release the stage at once, so that the ring refills while
+// they compute.  For index tiles lane L < 4G of warp w works on row 4w + L / G
+// and query head L mod G of the group.
 
 // Centroid-key tile: warp w scores rows 4w..4w+3 for the G heads of the group.
 template <int G>
@@ -1205,20 +1246,22 @@ __device__ __forceinline__ float kbar_dot(const DecodeArgs& a, const KbarRegs<G>
   }
   return reduce_scatter<4 * G>(v, lane);
 }
+// This lane's row and head of an index tile (lane L < 4G).
 template <int G>
-__device__ __forceinline__ void kbar_store(const DecodeArgs& a, float tot, int T, int4 n4,
+__device__ __forceinline__ int lane_row(int lane, int warp) {
+  return warp * 4 + (lane & (4 * G - 1)) / G;
+}
+template <int G>
+__device__ __forceinline__ int lane_head(int lane) {
+  return (lane & (4 * G - 1)) % G;
+}
+// n = the size of this lane's row (read from the stage before its release).
+template <int G>
+__device__ __forceinline__ void kbar_store(const DecodeArgs& a, float tot, const TileInfo& ti, int n,
                                            int lane, int warp) {
-  const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
-  const int nrows = min(kTile, a.C - c0);
-  const int L = lane & (4 * G - 1), j = L / G, h = L - j * G;
-  const int nx = __shfl_sync(kFull, n4.x, 0), ny = __shfl_sync(kFull, n4.y, 0);
-  const int nz = __shfl_sync(kFull, n4.z, 0), nw = __shfl_sync(kFull, n4.w, 0);
-  const int n = j == 0 ? nx : (j == 1 ? ny : (j == 2 ? nz : nw));
-  const int row = warp * 4 + j;
-  if (lane < 4 * G && row < nrows) {
-    const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-    a.scores[((size_t)b * a.Hq + g * G + h) * a.C + c0 + row] = n > 0 ? tot : -INFINITY;
-  }
+  const int row = lane_row<G>(lane, warp);
+  if (lane < 4 * G && row < ti.ntok)
+    a.scores[(size_t)(ti.h0 + lane_head<G>(lane)) * a.C + ti.c0 + row] = n > 0 ? tot : -INFINITY;
 }
 
 // Per-warp estimate state for the G heads of one KV group.
@@ -1249,22 +1292,13 @@ __device__ __forceinline__ void vsum_load(const DecSmem& S, int stage, int nrows
   }
 }
 
-// Value-sum tile: warp w accumulates rows 4w..4w+3.  Lane h < G holds s4, the
-// scores of head h for the 4 rows; lane 0 holds n4, their sizes.
+// Value-sum tile: warp w accumulates rows 4w..4w+3.  Lane L < 4G holds sj,
+// the score of its (row, head), and n, the row's size.
 template <int G>
-__device__ __forceinline__ void vsum_compute(const DecodeArgs& a, const float4 (&v)[4], int T,
-                                             float4 s4, int4 n4, EstState<G>& e, int lane,
-                                             int warp) {
-  const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
-  const int nrows = min(kTile, a.C - c0);
-  const int L = lane & (4 * G - 1), j = L / G, hL = L - j * G;
-  const float sx = __shfl_sync(kFull, s4.x, hL), sy = __shfl_sync(kFull, s4.y, hL);
-  const float sz = __shfl_sync(kFull, s4.z, hL), sw = __shfl_sync(kFull, s4.w, hL);
-  const float sj = j == 0 ? sx : (j == 1 ? sy : (j == 2 ? sz : sw));
-  const int nx = __shfl_sync(kFull, n4.x, 0), ny = __shfl_sync(kFull, n4.y, 0);
-  const int nz = __shfl_sync(kFull, n4.z, 0), nw = __shfl_sync(kFull, n4.w, 0);
-  const int n = j == 0 ? nx : (j == 1 ? ny : (j == 2 ? nz : nw));
-  const int row = warp * 4 + j;
+__device__ __forceinline__ void vsum_compute(const float4 (&v)[4], int nrows, float sj, int n,
+                                             EstState<G>& e, int lane, int warp) {
+  const int L = lane & (4 * G - 1), hL = L % G;
+  const int row = lane_row<G>(lane, warp);
   const float x = (lane < 4 * G && row < nrows && n > 0 && sj > -INFINITY) ? sj * kLog2e
                                                                             : -INFINITY;
   float mt = x;
@@ -1424,82 +1458,35 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     bad = cany(!ok) || bad;
     return !bad;
   };
-  // Every warp's scores of the previous tile were stored before the barrier
-  // of this tile's acquire: thread 0 publishes them with one count per warp.
-  auto signal_scored = [&](int bg) {
-    if (tid == 0) {
-      fence_gpu();
-      atomicAdd(a.grp_cnt + bg, (unsigned)kCW);
-    }
-  };
-  // Side data of tile T (T < 0: none) for the warp's 4 rows into slot
-  // i mod kSideSlots, i = the tile's position in the block's sequence (lane 0:
-  // the sizes; lane h < G: the scores of head h, stage 2 only).  Elements past
-  // the end of a group read as size 0 / score -inf.  One commit group per tile.
-  auto issue_side = [&](int T, int i, bool scores) {
-    if (T >= 0) {
-      SideSlot& sl = S.side[warp][i % kSideSlots];
-      const int bg = T / a.tpg, c = (T - bg * a.tpg) * kTile + warp * 4;
-      if (lane == 0) {
-        const int* p = a.size + (size_t)bg * a.C + c;
-        if (c + 4 <= a.C && ((uintptr_t)p & 15u) == 0) {
-          cp_async16(sl.n, p);
-        } else {
-          for (int k = 0; k < 4; ++k) {
-            if (c + k < a.C) cp_async4(sl.n + k, p + k);
-            else sl.n[k] = 0;
-          }
-        }
-      }
-      if (scores && lane < G) {
-        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-        const float* p = a.scores + ((size_t)b * a.Hq + g * G + lane) * a.C + c;
-        if (c + 4 <= a.C && ((uintptr_t)p & 15u) == 0) {
-          cp_async16(sl.s[lane], p);
-        } else {
-          for (int k = 0; k < 4; ++k) {
-            if (c + k < a.C) cp_async4(sl.s[lane] + k, p + k);
-            else sl.s[lane][k] = -INFINITY;
-          }
-        }
-      }
-    }
-    cp_async_commit();
-  };
-  // after cp_async_wait: lane 0 gets the sizes, lane h < G the scores of head h
-  auto side_sizes = [&](int i) -> int4 {
-    return lane == 0 ? *reinterpret_cast<const int4*>(S.side[warp][i % kSideSlots].n)
-                     : make_int4(0, 0, 0, 0);
-  };
-  auto side_scores = [&](int i) -> float4 {
-    return lane < G ? *reinterpret_cast<const float4*>(S.side[warp][i % kSideSlots].s[lane])
-                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  // this lane's size (and, for value-sum tiles, score) of a staged index tile
+  auto side_of = [&](int stage, int& n, float& sj) {
+    const int row = lane_row<G>(lane, warp);
+    n = S.sd[stage].n[row];
+    sj = S.sd[stage].s[lane_head<G>(lane)][row];
   };
 
   // ---- stage 1 (scoring blocks): scores
   if ((a.stages & kStageScore) && !sc.sel) {
-    auto T1 = [&](int i) { return i < sc.n1 ? sc.kj + i * sc.nk : -1; };
-    for (int i = 0; i < kSideAhead; ++i) issue_side(T1(i), i, false);
-    int prev_bg = -1;  // group of the previous tile, published after this tile's barrier
+    // Every warp stores its scores of tile i - 1 before the barrier of tile
+    // i's acquire; thread 0 then hands the count of stored tiles to the
+    // signaling warp, which publishes them on the groups' counters.
     for (int i = 0; i < sc.n1; ++i) {
-      const int T = sc.kj + i * sc.nk;
-      issue_side(T1(i + kSideAhead), i + kSideAhead, false);
       int stage;
       if (!acquire(stage)) break;
-      if (prev_bg >= 0) signal_scored(prev_bg);
+      if (tid == 0 && i > 0) st_release_cta(&S.scored, i);
+      const TileInfo ti = S.info[stage];
       KbarRegs<G> t;
-      const int c0 = (T % a.tpg) * kTile;
-      kbar_load<G>(S, stage, min(kTile, a.C - c0), t, lane, warp);
+      kbar_load<G>(S, stage, ti.ntok, t, lane, warp);
+      int n;
+      float unused;
+      side_of(stage, n, unused);
       release(stage);
-      cp_async_wait<kSideAhead>();
       const float tot = kbar_dot<G>(a, t, lane);
-      kbar_store<G>(a, tot, T, side_sizes(i), lane, warp);
-      prev_bg = T / a.tpg;
+      kbar_store<G>(a, tot, ti, n, lane, warp);
     }
-    cp_async_wait<0>();
-    if (!bad && prev_bg >= 0) {
+    if (!bad && sc.n1 > 0) {
       csync();
-      signal_scored(prev_bg);
+      if (tid == 0) st_release_cta(&S.scored, sc.n1);
     }
   }
 
@@ -1521,36 +1508,30 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         }
       }
     } else if (sc.v0 < sc.v1) {
-      for (int bg = sc.v0 / a.tpg; bg <= (sc.v1 - 1) / a.tpg; ++bg)
-        if (!wait_count(a.grp_cnt + bg, grp_target)) break;
-      if (!bad) {
-        EstState<G> e;
-        est_reset(e);
-        int cur_bg = -1, cur_n = 0;
-        const int n2 = sc.v1 - sc.v0;
-        for (int i = 0; i < kSideAhead; ++i) issue_side(i < n2 ? sc.v0 + i : -1, i, true);
-        for (int i = 0; i < n2; ++i) {
-          const int T = sc.v0 + i;
-          issue_side(i + kSideAhead < n2 ? T + kSideAhead : -1, i + kSideAhead, true);
-          const int bg = T / a.tpg;
-          if (bg != cur_bg) {  // same tiles in every warp: a uniform barrier
-            if (cur_bg >= 0) est_flush<G>(a, S, e, cur_bg, cur_n, lane);
-            cur_bg = bg;
-            cur_n = 0;
-          }
-          ++cur_n;
-          int stage;
-          if (!acquire(stage)) break;
-          float4 v[4];
-          const int c0 = (T % a.tpg) * kTile;
-          vsum_load(S, stage, min(kTile, a.C - c0), v, lane, warp);
-          release(stage);
-          cp_async_wait<kSideAhead>();
-          vsum_compute<G>(a, v, T, side_scores(i), side_sizes(i), e, lane, warp);
+      // (the producer stages a group's tiles once all of its scores are written)
+      EstState<G> e;
+      est_reset(e);
+      int cur_bg = sc.v0 / a.tpg, cur_n = 0, bg_end = (cur_bg + 1) * a.tpg;
+      for (int T = sc.v0; T < sc.v1; ++T) {
+        if (T == bg_end) {  // same tiles in every warp: a uniform barrier
+          est_flush<G>(a, S, e, cur_bg, cur_n, lane);
+          ++cur_bg;
+          cur_n = 0;
+          bg_end += a.tpg;
         }
-        cp_async_wait<0>();
-        if (!bad && cur_bg >= 0) est_flush<G>(a, S, e, cur_bg, cur_n, lane);
+        ++cur_n;
+        int stage;
+        if (!acquire(stage)) break;
+        float4 v[4];
+        vsum_load(S, stage, S.info[stage].ntok, v, lane, warp);
+        const int nrows = S.info[stage].ntok;
+        int n;
+        float sj;
+        side_of(stage, n, sj);
+        release(stage);
+        vsum_compute<G>(v, nrows, sj, n, e, lane, warp);
       }
+      if (!bad) est_flush<G>(a, S, e, cur_bg, cur_n, lane);
     }
   }
 
@@ -1604,6 +1585,38 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// signaling warp: publishes the block's scored index tiles on the KV groups'
+// counters (a gpu-scope fence per batch of tiles, off the consumers' path)
+// ---------------------------------------------------------------------------
+__device__ void signaler(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
+  if (sc.sel || sc.n1 == 0 || !(a.stages & kStageScore)) return;
+  const int lane = threadIdx.x & 31;
+  int done = 0;
+  while (done < sc.n1) {
+    int c = done;
+    if (lane == 0) {
+      const unsigned long long t0 = global_ns();
+      for (;;) {
+        c = ld_acquire_cta(&S.scored);
+        if (c > done) break;
+        if (*(volatile int*)&S.abort || global_ns() - t0 > kWaitLimitNs) {
+          c = -1;  // the consumers gave up (and reported why)
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    c = __shfl_sync(kFull, c, 0);
+    if (c < 0) return;
+    __syncwarp();
+    fence_gpu();  // the consumers' score stores before the counts
+    for (int j = done + lane; j < c; j += 32)
+      atomicAdd(a.grp_cnt + (sc.kj + j * sc.nk) / a.tpg, (unsigned)kCW);
+    done = c;
+  }
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1619,10 +1632,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     S.issued = 0;
     S.confirmed = 0;
     S.flag = 0;
+    S.scored = 0;
   }
   __syncthreads();
   const Sched sc = schedule(a, blockIdx.x);
-  if (tid >= kCT) producer<G>(a, S, sc);
+  if (tid >= kCT + 32) signaler(a, S, sc);
+  else if (tid >= kCT) producer<G>(a, S, sc);
   else consumers<G>(a, S, sc);
   __syncthreads();
   if (tid == 0) {

@@ -137,6 +137,16 @@ def test_gqa_groups_ragged(G):
     check_decode(g, oidx, ix, r=10)
 
 
+def test_odd_cluster_count():
+    # C = 5 * 33 = 165: rows of sizes and scores do not start on 16-byte
+    # boundaries, so their side data is staged with plain loads; the last
+    # index tile of a group is ragged (37 rows)
+    g, oidx = random_case(31, B=2, Hq=4, Hkv=2, N=5000, sink=4, window=64, seg_len=1024, k=33,
+                          assign_mode="random")
+    ix = gpu_index(g, oidx, 4, 64, 1024, 33)
+    check_decode(g, oidx, ix, r=20)
+
+
 @pytest.mark.parametrize("r", [0, 1, 37, 160])
 def test_budget_edges(r):
     # C = 5 * 32 = 160; r = C retrieves every non-empty cluster
