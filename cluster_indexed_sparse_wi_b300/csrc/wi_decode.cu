@@ -98,6 +98,19 @@ struct __align__(16) StageSide {
   float s[8][kTile];
 };
 
+// A request to the signaling warp: after a gpu-scope fence (covering every
+// write the consumers made before queueing it), add val to *cnt (kPubAdd),
+// set *cnt = val (kPubSet), or add val to head bh's arrival counter and queue
+// the head for merging in this block if that completes it (kPubPiece).
+enum : int { kPubAdd = 0, kPubSet = 1, kPubPiece = 2 };
+struct PubReq {
+  unsigned* cnt;
+  unsigned val;
+  int op, bh, pad;
+};
+constexpr int kPubSlots = 16;
+constexpr int kMergeSlots = 32;  // > kPubSlots + 1: merges queued before the consumers drain them
+
 struct __align__(128) DecSmem {
   unsigned char ring[kStages][kStageBytes];  // bulk-copy destinations (16-byte aligned)
   StageSide sd[kStages];
@@ -116,13 +129,21 @@ struct __align__(128) DecSmem {
   int2 scan[2][kCW];
   int sel_i[4];
   uint32_t red_u[2][kCW];
-  uint32_t sel_hand[8];
   uint32_t win_sum[2][kCW][kNumWindows / 2];
   int abort;              // some wait of this block gave up
   int issued;             // tiles whose copies the producer issued
   int confirmed;          // tiles whose full barrier the consumers saw complete
   int flag;
   int scored;             // stage-1 tiles whose scores every consumer warp has stored
+  PubReq pub[kPubSlots];  // requests to the signaling warp (ring)
+  int merge_q[kMergeSlots];  // heads this block merges (ring)
+  int pub_tail;           // requests queued (consumer thread 0)
+  int pub_head;           // requests done (signaling warp)
+  int merge_tail;         // heads queued for merging (signaling warp)
+  int mt_snap[2];         // merge_tail as seen before tile barriers (by parity of the tile)
+  int mt_final;           // merge_tail once the signaling warp has finished
+  int cons_done;          // the consumers queue no more requests
+  int sig_done;           // the signaling warp has finished
 };
 static_assert(offsetof(DecSmem, qs) % 16 == 0, "bulk-copy alignment");
 static_assert(offsetof(DecSmem, sd) % 16 == 0, "bulk-copy alignment");
@@ -256,9 +277,8 @@ __device__ Sched schedule(const DecodeArgs& a, int b) {
 
 // Combine the 16 consumer warps' (m, l, o) into one partial at dst:
 // dst[0] = m (log2 units), dst[1] = sign * l, dst[2..] = sign * o.
-// m and l are warp-uniform; o holds this lane's 4 dimensions.  The writing
-// threads fence before the closing barrier, so that one thread may publish the
-// partial with a counter right after it.
+// m and l are warp-uniform; o holds this lane's 4 dimensions.  Ends with a
+// consumer barrier, after which the partial may be published.
 __device__ void combine_write(DecSmem& S, float m, float l, float4 o, float* dst, float sign) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (lane == 0) {
@@ -286,7 +306,6 @@ __device__ void combine_write(DecSmem& S, float m, float l, float4 o, float* dst
       dst[1] = sign * L;
     }
     dst[2 + tid] = sign * O;
-    fence_gpu();
   }
   csync();
 }
@@ -326,108 +345,24 @@ __device__ int2 cscan2(int2 v, DecSmem& S, int2* total, int& buf) {
 }
 
 // ---------------------------------------------------------------------------
-// The r-th largest of n <= kCT distinct 64-bit values v[0..n) in shared
-// memory (1 <= r <= n), by all consumer threads (thread t holds v[t]): radix
-// select with 11-bit digits from the highest bit in which the values differ;
-// histograms of 2048 counters in `hist` (shared), boundary digit by a block
-// scan.  About two passes for values that differ in their top bits.
-__device__ unsigned long long block_select_desc(DecSmem& S, const unsigned long long* v, int n,
-                                                int r, int* hist, int& buf) {
-  constexpr int kDig = 11, kNb = 1 << kDig, kPer = kNb / kCT;  // 4 digits per thread
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool has = tid < n;
-  const unsigned long long mine = has ? v[tid] : 0ull, v0 = v[0];
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(S.red_o[0]);  // [2][kCW][2]
-  auto block_or_min = [&](unsigned long long x, unsigned long long y, unsigned long long& xo,
-                          unsigned long long& yo) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      x |= __shfl_xor_sync(kFull, x, o);
-      const unsigned long long t = __shfl_xor_sync(kFull, y, o);
-      y = t < y ? t : y;
-    }
-    unsigned long long* rb = red + (size_t)buf * 2 * kCW;
-    buf ^= 1;
-    if (lane == 0) {
-      rb[2 * warp] = x;
-      rb[2 * warp + 1] = y;
-    }
-    csync();
-    xo = 0ull;
-    yo = ~0ull;
-#pragma unroll
-    for (int w = 0; w < kCW; ++w) {
-      xo |= rb[2 * w];
-      yo = rb[2 * w + 1] < yo ? rb[2 * w + 1] : yo;
-    }
-  };
-  unsigned long long diff, lo;
-  block_or_min(has ? (mine ^ v0) : 0ull, has ? mine : ~0ull, diff, lo);
-  if (r == n || diff == 0ull) return lo;  // every value taken
-  int bit = 63 - __clzll(diff);
-  unsigned long long mask = bit == 63 ? 0ull : (~0ull << (bit + 1));
-  unsigned long long prefix = v0 & mask;
-  int remaining = r;
-  uint32_t* hand = S.sel_hand;
-  for (int pass = 0;; ++pass) {
-    const int width = min(kDig, bit + 1), shift = bit + 1 - width;
-    const unsigned long long dm = (1ull << width) - 1ull;
-    const int nbins = 1 << width;
-    for (int i = tid; i < nbins; i += kCT) hist[i] = 0;
-    csync();
-    if (has && (mine & mask) == prefix) atomicAdd(&hist[(int)((mine >> shift) & dm)], 1);
-    csync();
-    // thread t owns the kPer digits [hi - kPer, hi) counted from the top
-    const int bhi = nbins - kPer * tid, blo = max(0, bhi - kPer);
-    int own = 0;
-    if (bhi > 0)
-      for (int i = blo; i < bhi; ++i) own += hist[i];
-    int2 tot;
-    const int excl = cscan2(make_int2(own, 0), S, &tot, buf).x;
-    uint32_t* hd = hand + 2 * (pass & 1);  // hand[0..1] / hand[2..3], alternating
-    if (own > 0 && excl < remaining && remaining <= excl + own) {
-      int acc = excl;
-      for (int i = bhi - 1; i >= blo; --i) {
-        const int c = hist[i];
-        if (acc + c >= remaining) {
-          hd[0] = (uint32_t)i | ((uint32_t)c << 16);
-          hd[1] = (uint32_t)acc;
-          break;
-        }
-        acc += c;
-      }
-    }
-    csync();
-    const int D = (int)(hd[0] & 0xffffu), cntD = (int)(hd[0] >> 16), above = (int)hd[1];
-    remaining -= above;
-    prefix |= (unsigned long long)D << shift;
-    mask |= dm << shift;
-    if (cntD == remaining || shift == 0) {
-      // every value of the boundary digit is taken: the smallest of them
-      unsigned long long dummy, m;
-      block_or_min(0ull, (has && (mine & mask) == prefix) ? mine : ~0ull, dummy, m);
-      return m;
-    }
-    bit = shift - 1;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // selection of one query head (all 512 consumers)
 // ---------------------------------------------------------------------------
-// T = the r_eff = min(r, non-empty) largest scores, ties to the lower id.  T is
-// found as a threshold on (key, id): a cluster with order-preserving key k is
-// selected iff k > Kb, or k == Kb and its id <= cb.  Keys are held in
-// registers, 16 consecutive ids per thread.  One pass histograms the keys'
-// top 12 bits (4096 digits; a larger key never has a smaller digit); the digit
-// D holding the r_eff-th largest key follows from a scan from the top, every
-// cluster with a larger digit is selected, and the candidates with digit D are
-// ranked exactly by (key desc, id asc) to give (Kb, cb).  When digit D holds
-// more than kCand candidates an exact radix select over the keys gives
-// (Kb, cb) instead.  The selected ids are compacted in ascending order; one
-// round of independent loads then fetches each cluster's size, first sorted
-// row and value-sum row for the outputs and for the estimate of T (kept with
-// a negative sign).
+// T = the r_eff = min(r, non-empty) largest scores, ties to the lower id.
+// Keys (order-preserving images of the scores, 0 = empty cluster) are held in
+// registers, 16 consecutive ids per thread.
+//   Up to 8192 clusters: after one barrier for the count and range of the
+//   keys, one pass counts the keys of 8 windows below the largest (2, 4, ...,
+//   16 digits of the top 12 key bits) and one block scan of those counts
+//   gives every thread its place in each window.  The smallest window holding
+//   at least r_eff keys is gathered in id order (at most 512 candidates) and
+//   each candidate counts the candidates ranked above it by (key desc, id
+//   asc): it is selected iff fewer than r_eff are.  A last scan writes the
+//   selected ids ascending with their clusters' sizes and first sorted rows,
+//   loaded while the ranks are counted.
+//   Otherwise (more clusters, or no window small enough): an exact radix
+//   select over the keys, 12 bits per pass, gives a threshold (Kb, cb) -- a
+//   cluster is selected iff k > Kb, or k == Kb and its id <= cb -- and a
+//   compaction pass over all keys writes the selection.
 template <int G>
 __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -486,7 +421,6 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
     kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
   }
-  uint32_t* hand = S.sel_hand;
   {
     int2* sh = S.scan[buf];
     buf ^= 1;
@@ -495,7 +429,6 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       S.red_u[0][warp] = kmax;
       S.red_u[1][warp] = kmin;
     }
-    if (tid == 0) hand[3] = 0u;  // candidate counter
     csync();
     valid = 0;
     kmax = 0u;
@@ -517,76 +450,132 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     Kb = 0u;  // every non-empty cluster
   } else if (r_eff > 0) {
     bool done = false;
-    int win = -1, win_total = 0;
-    // Candidates: keys whose top 12 bits (d = k >> 20) lie within w digits of
-    // the largest key's, d_max - d <= w, for the smallest w of 2, 4, ..., 16 that
-    // holds at least r_eff keys (one counting pass, all windows at once).  When
-    // they number at most kCT, a radix select over them finds the r_eff-th
-    // largest (key desc, id asc).
-    const uint32_t dmax = kmax >> 20;
-    // per-thread counts of the windows, one byte each (at most 16 keys): a
-    // key o digits below the largest is in windows w >= w0(o)
-    unsigned long long cw64 = 0ull;
-    visit([&](uint32_t k, int) {
-      const uint32_t o = dmax - (k >> 20);  // digits below the largest
-      const uint32_t w0 = o <= 2u ? 0u : min((o - 1u) >> 1, 8u);  // 8: in no window
-      const unsigned long long inc = w0 < 8u ? (0x0101010101010101ull << (8u * w0)) : 0ull;
-      cw64 += k != 0u ? inc : 0ull;
-    });
-    const uint32_t cw[2] = {(uint32_t)cw64, (uint32_t)(cw64 >> 32)};
-    {
-      // block totals (at most 8192 each): two 16-bit fields per word
+    if (nch == 1) {
+      // Candidates: keys whose top 12 bits (d = k >> 20) lie within w digits
+      // of the largest key's, d_max - d <= w, for the smallest w of 2, 4, ..., 16
+      // that holds at least r_eff keys.  One pass counts every window and one
+      // block scan of the counts gives each thread its gather position in all
+      // of them.
+      const uint32_t dmax = kmax >> 20;
+      // per-thread counts of the windows, one byte each (at most 16 keys): a
+      // key o digits below the largest is in windows w >= w0(o)
+      unsigned long long cw64 = 0ull;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t k = k0[j];
+        const uint32_t o = dmax - (k >> 20);
+        const uint32_t w0 = o <= 2u ? 0u : min((o - 1u) >> 1, 8u);  // 8: in no window
+        const unsigned long long inc = w0 < 8u ? (0x0101010101010101ull << (8u * w0)) : 0ull;
+        cw64 += k != 0u ? inc : 0ull;
+      }
+      // windows 2x and 2x+1 as two 16-bit fields of word x (block totals <= 8192)
+      uint32_t own[4], incl[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const uint32_t c = (uint32_t)(cw64 >> (16 * x));
+        own[x] = (c & 0xffu) | ((c >> 8 & 0xffu) << 16);
+        incl[x] = own[x];
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t t = __shfl_up_sync(kFull, incl[x], o);
+          if (lane >= o) incl[x] += t;
+        }
+      }
       uint32_t(*wsum)[kNumWindows / 2] =
           reinterpret_cast<uint32_t(*)[kNumWindows / 2]>(S.win_sum[buf]);
       buf ^= 1;
-#pragma unroll 1
-      for (int x = 0; x < kNumWindows / 2; ++x) {
-        const uint32_t c = (x < 2 ? cw[0] : cw[1]) >> (16 * (x % 2));
-        uint32_t pk = (c & 0xffu) | ((c >> 8 & 0xffu) << 16);
+      if (lane == 31) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) pk += __shfl_xor_sync(kFull, pk, o);
-        if (lane == 0) wsum[warp][x] = pk;
+        for (int x = 0; x < 4; ++x) wsum[warp][x] = incl[x];
       }
       csync();
-#pragma unroll 1
-      for (int x = kNumWindows / 2 - 1; x >= 0; --x) {
-        uint32_t t = 0u;
+      uint32_t base[4] = {0u, 0u, 0u, 0u}, tot[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int y = 0; y < kCW; ++y) t += wsum[y][x];
-        const int hi = (int)(t >> 16), lo = (int)(t & 0xffffu);  // windows 2x+1, 2x
-        if (hi >= r_eff) {
-          win = 2 * x + 1;
-          win_total = hi;
-        }
-        if (lo >= r_eff) {
-          win = 2 * x;
-          win_total = lo;
+      for (int y = 0; y < kCW; ++y) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t t = wsum[y][x];
+          if (y < warp) base[x] += t;
+          tot[x] += t;
         }
       }
-    }
-    const uint32_t wsel = win >= 0 ? window_digits(win) : 0u;
-    int nc = 0;
+      int win = -1, n_cand = 0;
 #pragma unroll
-    for (int w = 0; w < kNumWindows; ++w)
-      if (w == win) nc = (int)((cw[w / 4] >> (8 * (w % 4))) & 0xffu);
-    auto in_window = [&](uint32_t k) { return k != 0u && dmax - (k >> 20) <= wsel; };
-    // candidates as composites (key << 32 | ~id): larger composite = selected
-    // first; unique since ids are
-    unsigned long long* cand = reinterpret_cast<unsigned long long*>(S.u.hist);
-    int2 ctot;
-    int cpos = cscan2(make_int2(nc, 0), S, &ctot, buf).x;
-    const int n_cand = win >= 0 ? win_total : 0;
-    if (n_cand >= r_eff && n_cand <= kCT) {
-      visit([&](uint32_t k, int c) {
-        if (in_window(k))
-          cand[cpos++] = ((unsigned long long)k << 32) | (unsigned long long)(0xffffffffu - (uint32_t)c);
-      });
-      csync();
-      const unsigned long long T = block_select_desc(S, cand, n_cand, r_eff,
-                                                     reinterpret_cast<int*>(cand + kCT), buf);
-      Kb = (uint32_t)(T >> 32);
-      cb = (int)(0xffffffffu - (uint32_t)T);
-      done = true;
+      for (int w = kNumWindows - 1; w >= 0; --w) {
+        const int t = (int)((tot[w / 2] >> (16 * (w % 2))) & 0xffffu);
+        if (t >= r_eff) {
+          win = w;
+          n_cand = t;
+        }
+      }
+      if (win >= 0 && n_cand <= kCT) {
+        // gather the candidates in id order as composites (key << 32 | ~id):
+        // a larger composite is selected first; unique since the ids are
+        uint32_t pos = 0u;
+#pragma unroll
+        for (int w = 0; w < kNumWindows; ++w)
+          if (w == win)
+            pos = ((base[w / 2] + incl[w / 2] - own[w / 2]) >> (16 * (w % 2))) & 0xffffu;
+        const uint32_t wsel = window_digits(win);
+        unsigned long long* cand = reinterpret_cast<unsigned long long*>(S.u.hist);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t k = k0[j];
+          if (k != 0u && dmax - (k >> 20) <= wsel)
+            cand[pos++] = ((unsigned long long)k << 32) | (unsigned long long)(0xffffffffu - (uint32_t)(tid * 16 + j));
+        }
+        csync();
+        // Thread t < n_cand ranks candidate t against all of them; its
+        // cluster's size and first sorted row are loaded meanwhile.
+        const bool has = tid < n_cand;
+        const unsigned long long mine = has ? cand[tid] : 0ull;
+        const int cid = (int)(0xffffffffu - (uint32_t)mine);
+        int nj = 0, rowj = 0;
+        if (has) {
+          nj = __ldg(sz + cid);
+          rowj = __ldg(off + cid);
+        }
+        int rank = 0;
+        if (has) {
+          const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
+          const int half = n_cand >> 1;
+#pragma unroll 4
+          for (int j = 0; j < half; ++j) {
+            const ulonglong2 v = c2[j];
+            rank += (int)(v.x > mine) + (int)(v.y > mine);
+          }
+          if (n_cand & 1) rank += (int)(cand[n_cand - 1] > mine);
+        }
+        const bool take = has && rank < r_eff;
+        int2 ptot;
+        const int p = cscan2(make_int2(take ? 1 : 0, 0), S, &ptot, buf).x;  // ids ascending
+        int* ids = a.sel_ids + (size_t)bh * rs;
+        int* rows = a.sel_rows + (size_t)bh * rs;
+        int* cnts = a.sel_cnts + (size_t)bh * rs;
+        int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
+        if (take) {
+          if (nj < 0 || rowj < 0 || (long long)rowj + nj > a.N_idx) {
+            report(a.status, WI_ERR_INDEX_MISMATCH);  // inconsistent index: stage nothing
+            nj = 0;
+            rowj = 0;
+          }
+          ids[p] = cid;
+          rows[p] = rowj;
+          cnts[p] = nj;
+          if (topk) topk[p] = cid;
+        }
+        for (int i = r_eff + tid; i < rs; i += kCT) {
+          ids[i] = -1;
+          rows[i] = 0;
+          cnts[i] = 0;
+          if (topk && i < r) topk[i] = -1;
+        }
+        csync();  // the selection is published after this barrier
+        return;
+      }
     }
     if (!done) {
       // exact radix select over the keys, 12 bits per pass from the highest
@@ -753,8 +742,7 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       cnts[j] = nj;
     }
   }
-  fence_gpu();  // the selection is published with a counter after this barrier
-  csync();
+  csync();  // the selection is published after this barrier
 }
 
 // The estimate of one head's selected clusters (kept with a negative sign):
@@ -1335,11 +1323,10 @@ __device__ __forceinline__ void vsum_compute(const float4 (&v)[4], int nrows, fl
   }
 }
 
-// Writes the block's estimate piece of group bg (ntiles of its tiles) and
-// counts the tiles on the group's counter.
+// Writes the block's estimate piece of group bg (ntiles of its tiles); the
+// caller publishes it.
 template <int G>
-__device__ void est_flush(const DecodeArgs& a, DecSmem& S, EstState<G>& e, int bg, int ntiles,
-                          int lane) {
+__device__ void est_flush(const DecodeArgs& a, DecSmem& S, EstState<G>& e, int bg, int lane) {
   const int L = lane & (4 * G - 1);
   const int hL = L % G;
 #pragma unroll
@@ -1348,7 +1335,6 @@ __device__ void est_flush(const DecodeArgs& a, DecSmem& S, EstState<G>& e, int b
     float* dst = a.est_part + ((size_t)(blockIdx.x + bg) * G + h) * kPartStride;
     combine_write(S, e.m[h], lh, e.o[h], dst, 1.f);
   }
-  if (threadIdx.x == 0) atomicAdd(a.est_cnt + bg, (unsigned)ntiles);
   est_reset(e);
 }
 
@@ -1436,9 +1422,36 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
            mbar_wait(smem_addr(&S.full[stage]), (seq / kStages) & 1u, a.status);
       if (ok) S.confirmed = (int)(seq + 1);
       else S.abort = 1;
+      // double-buffered: a warp may still read the previous tile's copy
+      S.mt_snap[seq & 1u] = ld_acquire_cta(&S.merge_tail);
     }
     bad = cany(!ok);
     return !bad;
+  };
+  // Queue a request to the signaling warp (thread 0; every consumer calls it
+  // after the barrier that follows the writes it publishes).
+  auto publish = [&](unsigned* cnt, unsigned val, int op, int bh) {
+    if (tid == 0) {
+      const int t = S.pub_tail;
+      if (t - ld_acquire_cta(&S.pub_head) >= kPubSlots) {  // ring full: wait (bounded)
+        const unsigned long long t0 = global_ns();
+        while (t - ld_acquire_cta(&S.pub_head) >= kPubSlots) {
+          if (*(volatile int*)&S.abort) break;
+          if (global_ns() - t0 > kWaitLimitNs) {
+            report(a.status, WI_ERR_DEVICE_TIMEOUT);
+            S.abort = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      PubReq& q = S.pub[t % kPubSlots];
+      q.cnt = cnt;
+      q.val = val;
+      q.op = op;
+      q.bh = bh;
+      st_release_cta(&S.pub_tail, t + 1);
+    }
   };
   // release a stage whose data this warp has copied to registers
   auto release = [&](int stage) {
@@ -1457,6 +1470,24 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     }
     bad = cany(!ok) || bad;
     return !bad;
+  };
+  // a head merges once its group's estimate pieces and its negative estimate
+  // are written
+  auto merge_ready = [&](int bh) -> bool {
+    const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+    return wait_count(a.est_cnt + (size_t)b * a.Hkv + g, (unsigned)a.tpg) &&
+           wait_count(a.neg_ready + bh, 1u);
+  };
+  // Merge the heads whose last piece this block published, up to mt (queued
+  // by the signaling warp; mt was read by thread 0 before the barrier that
+  // precedes every call).
+  int merges_done = 0;
+  auto drain_merges = [&](int mt) {
+    while (merges_done < mt && !bad) {
+      const int bh = S.merge_q[merges_done % kMergeSlots];
+      ++merges_done;
+      if (merge_ready(bh)) merge_head<G>(a, S, bh);
+    }
   };
   // this lane's size (and, for value-sum tiles, score) of a staged index tile
   auto side_of = [&](int stage, int& n, float& sj) {
@@ -1498,13 +1529,13 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
         if (!wait_count(a.grp_cnt + (size_t)b * a.Hkv + g, grp_target)) break;
         select_head<G>(a, S, bh);
-        if (tid == 0) atomicExch(a.sel_ready + bh, 1u);
+        publish(a.sel_ready + bh, 1u, kPubSet, bh);
       }
       // the estimates of this block's selections, published per head
       if (!bad) {
         for (int bh = sc.sel0; bh < H; bh += sc.sel_step) {
           estimate_selected<G>(a, S, bh);
-          if (tid == 0) atomicExch(a.neg_ready + bh, 1u);
+          publish(a.neg_ready + bh, 1u, kPubSet, bh);
         }
       }
     } else if (sc.v0 < sc.v1) {
@@ -1514,7 +1545,8 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
       int cur_bg = sc.v0 / a.tpg, cur_n = 0, bg_end = (cur_bg + 1) * a.tpg;
       for (int T = sc.v0; T < sc.v1; ++T) {
         if (T == bg_end) {  // same tiles in every warp: a uniform barrier
-          est_flush<G>(a, S, e, cur_bg, cur_n, lane);
+          est_flush<G>(a, S, e, cur_bg, lane);
+          publish(a.est_cnt + cur_bg, (unsigned)cur_n, kPubAdd, 0);
           ++cur_bg;
           cur_n = 0;
           bg_end += a.tpg;
@@ -1531,24 +1563,21 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         release(stage);
         vsum_compute<G>(v, nrows, sj, n, e, lane, warp);
       }
-      if (!bad) est_flush<G>(a, S, e, cur_bg, cur_n, lane);
+      if (!bad) {
+        est_flush<G>(a, S, e, cur_bg, lane);
+        publish(a.est_cnt + cur_bg, (unsigned)cur_n, kPubAdd, 0);
+      }
     }
   }
 
   // ---- stage 3: exact attention over steady and retrieved rows, merges
   if ((a.stages & kStageAttend) && !bad) {
-    // a head merges once its group's estimate pieces and its negative estimate
-    // are written
-    auto merge_ready = [&](int bh) -> bool {
-      const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
-      return wait_count(a.est_cnt + (size_t)b * a.Hkv + g, (unsigned)a.tpg) &&
-             wait_count(a.neg_ready + bh, 1u);
-    };
     AttState st = {-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
     const int per_head = a.tph + a.r;
     for (;;) {
       int stage;
       if (!acquire(stage)) break;
+      drain_merges(S.mt_snap[seq & 1u]);
       const TileInfo t = S.info[stage];
       if (t.kind == kTileEnd) {
         release(stage);
@@ -1565,16 +1594,7 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         st.m = -INFINITY;
         st.l = 0.f;
         st.o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (tid == 0) {
-          const unsigned old = atomicAdd(a.head_cnt + t.bh, (unsigned)t.units);
-          S.flag = (old + (unsigned)t.units == (unsigned)per_head);
-          if (S.flag) fence_gpu();  // the other pieces before this block's loads
-        }
-        csync();
-        if (S.flag) {
-          if (merge_ready(t.bh)) merge_head<G>(a, S, t.bh);
-          if (bad) break;
-        }
+        publish(a.head_cnt + t.bh, (unsigned)t.units, kPubPiece, t.bh);
       }
     }
     // heads with no steady tile and no retrieval budget: one designated block
@@ -1583,38 +1603,83 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         if (merge_ready((int)bh)) merge_head<G>(a, S, (int)bh);
     }
   }
+  // No more requests; the signaling warp's last batch may still complete a
+  // head that this block then merges.
+  if (tid == 0) {
+    st_release_cta(&S.cons_done, 1);
+    const unsigned long long t0 = global_ns();
+    while (!ld_acquire_cta(&S.sig_done)) {
+      if (global_ns() - t0 > kWaitLimitNs) {
+        report(a.status, WI_ERR_DEVICE_TIMEOUT);
+        S.abort = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    S.mt_final = ld_acquire_cta(&S.merge_tail);
+  }
+  csync();
+  if (a.stages & kStageAttend) drain_merges(S.mt_final);
 }
 
 // ---------------------------------------------------------------------------
-// signaling warp: publishes the block's scored index tiles on the KV groups'
-// counters (a gpu-scope fence per batch of tiles, off the consumers' path)
+// signaling warp: publishes the block's results on the grid's counters -- the
+// scored index tiles on the KV groups' counters and the consumers' queued
+// requests -- with one gpu-scope fence per batch, off the consumers' path.
+// A piece that completes its head queues the head's merge for this block.
 // ---------------------------------------------------------------------------
 __device__ void signaler(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
-  if (sc.sel || sc.n1 == 0 || !(a.stages & kStageScore)) return;
   const int lane = threadIdx.x & 31;
-  int done = 0;
-  while (done < sc.n1) {
-    int c = done;
+  const int n1 = (!sc.sel && (a.stages & kStageScore)) ? sc.n1 : 0;
+  const unsigned per_head = (unsigned)(a.tph + a.r);
+  int done1 = 0, ph = 0;
+  for (;;) {
+    int c1 = done1, pt = ph, fin = 0;
     if (lane == 0) {
       const unsigned long long t0 = global_ns();
       for (;;) {
-        c = ld_acquire_cta(&S.scored);
-        if (c > done) break;
+        fin = ld_acquire_cta(&S.cons_done);  // first: what was queued before it is seen below
+        c1 = n1 > 0 ? ld_acquire_cta(&S.scored) : 0;
+        pt = ld_acquire_cta(&S.pub_tail);
+        if (c1 > done1 || pt > ph || fin) break;
         if (*(volatile int*)&S.abort || global_ns() - t0 > kWaitLimitNs) {
-          c = -1;  // the consumers gave up (and reported why)
+          c1 = -1;  // the consumers gave up (and reported why)
           break;
         }
         __nanosleep(64);
       }
     }
-    c = __shfl_sync(kFull, c, 0);
-    if (c < 0) return;
+    c1 = __shfl_sync(kFull, c1, 0);
+    pt = __shfl_sync(kFull, pt, 0);
+    fin = __shfl_sync(kFull, fin, 0);
+    if (c1 < 0) break;
     __syncwarp();
-    fence_gpu();  // the consumers' score stores before the counts
-    for (int j = done + lane; j < c; j += 32)
+    if (c1 == done1 && pt == ph) break;  // fin: nothing more will come
+    fence_gpu();  // every write the consumers made before these requests
+    for (int j = done1 + lane; j < c1; j += 32)
       atomicAdd(a.grp_cnt + (sc.kj + j * sc.nk) / a.tpg, (unsigned)kCW);
-    done = c;
+    if (lane == 0) {
+      for (int i = ph; i < pt; ++i) {
+        const PubReq q = S.pub[i % kPubSlots];
+        if (q.op == kPubSet) {
+          atomicExch(q.cnt, q.val);
+        } else {
+          const unsigned old = atomicAdd(q.cnt, q.val);
+          if (q.op == kPubPiece && old + q.val == per_head) {
+            fence_gpu();  // the other blocks' pieces before this block's merge reads them
+            const int mt = S.merge_tail;
+            S.merge_q[mt % kMergeSlots] = q.bh;
+            st_release_cta(&S.merge_tail, mt + 1);
+          }
+        }
+      }
+      st_release_cta(&S.pub_head, pt);
+    }
+    __syncwarp();
+    done1 = c1;
+    ph = pt;
   }
+  if (lane == 0) st_release_cta(&S.sig_done, 1);
 }
 
 template <int G>
@@ -1633,6 +1698,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     S.confirmed = 0;
     S.flag = 0;
     S.scored = 0;
+    S.pub_tail = S.pub_head = S.merge_tail = S.mt_final = 0;
+    S.mt_snap[0] = S.mt_snap[1] = 0;
+    S.cons_done = S.sig_done = 0;
   }
   __syncthreads();
   const Sched sc = schedule(a, blockIdx.x);
