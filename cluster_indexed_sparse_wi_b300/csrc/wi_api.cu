@@ -278,17 +278,17 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->nb = nb;
   a->tpg = tpg;
   a->tph = (p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile;
-  // Blocks [0, nsel) select (heads dealt round robin); the others score the
-  // index tiles (a centroid-key and a value-sum tile each).  The split
+  // Blocks [0, nsel) select (heads dealt round robin); the others stream the
+  // value-sum tiles (every block scores centroid-key tiles).  The split
   // minimises the larger of the two loads, a selection costing about
-  // selection_weight() centroid-key tiles.
+  // selection_weight() tiles.
   const long long H = (long long)p->B * p->Hq;
   const double wsel = selection_weight(C);
   int best = 1;
   double best_cost = 1e300;
   for (int ns = 1; ns <= nb - 1 && ns <= H; ++ns) {
     const double sel = (double)((H + ns - 1) / ns) * wsel;
-    const double idx = 2.0 * (double)((n_tiles + (nb - ns) - 1) / (nb - ns));
+    const double idx = (double)((n_tiles + (nb - ns) - 1) / (nb - ns));
     const double cost = sel > idx ? sel : idx;
     if (cost < best_cost) {
       best_cost = cost;

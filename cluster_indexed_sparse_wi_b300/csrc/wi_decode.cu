@@ -10,7 +10,7 @@
 // (cp.async.bulk + mbarrier complete_tx); the consumers compute on the staged
 // tiles.  Blocks [0, nsel) are selection blocks, the others scoring blocks.
 //
-//   stage 1  (scoring blocks) centroid-key tiles (64 rows of kbar, f32) with
+//   stage 1  (all blocks) centroid-key tiles (64 rows of kbar, f32) with
 //            the group's query rows, in KV-group order, dealt round robin:
 //              s[b,h,c] = scale q_h . kbar_c (-inf if n_c = 0)   -> scores
 //            every warp counts its finished tiles on the group's counter;
@@ -245,8 +245,9 @@ __device__ __forceinline__ int part_owner(long long p, long long len, int nb) {
 struct Sched {
   bool sel;                    // a selection block
   int sel0, sel_step;          // its heads sel0, sel0 + sel_step, ... < B*Hq
-  int kj, nk, n1;              // scoring block kj of nk: centroid-key tiles kj + i*nk, i < n1
-  int v0, v1;                  // its value-sum tiles [v0, v1)
+  int k0, kstep, n1;           // centroid-key tiles k0 + i*kstep, i < n1 (every block)
+  int kj, nk;                  // scoring block kj of nk ...
+  int v0, v1;                  // ... and its value-sum tiles [v0, v1)
   long long s0, s1;            // steady tiles
   long long r0, r1;            // retrieved slots
 };
@@ -259,10 +260,13 @@ __device__ Sched schedule(const DecodeArgs& a, int b) {
   s.sel_step = a.nsel;
   s.nk = a.nb - a.nsel;
   s.kj = b - a.nsel;
-  s.n1 = 0;
+  // centroid-key tiles are dealt round robin over all blocks in KV-group
+  // order (the selection blocks have nothing else to do until a group is done)
+  s.k0 = b;
+  s.kstep = a.nb;
+  s.n1 = b < nt ? (int)((nt - b + a.nb - 1) / a.nb) : 0;
   s.v0 = s.v1 = 0;
   if (!s.sel) {
-    s.n1 = s.kj < nt ? (int)((nt - s.kj + s.nk - 1) / s.nk) : 0;
     s.v0 = (int)part_lo(s.kj, nt, s.nk);
     s.v1 = (int)part_lo(s.kj + 1, nt, s.nk);
   }
@@ -990,18 +994,18 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     else bulk_g2s(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]));
   };
 
-  // stages 1 and 2 (scoring blocks): centroid-key tiles kj, kj + nk, ...
-  // with the group's query rows and the clusters' sizes; then the value-sum
-  // tiles [v0, v1) with the sizes and the group's scores (each group's once
-  // every score of it is written)
+  // stage 1 (every block): centroid-key tiles k0, k0 + kstep, ...
+  // with the group's query rows and the clusters' sizes; then (scoring
+  // blocks) the value-sum tiles [v0, v1) with the sizes and the group's
+  // scores (each group's once every score of it is written)
   const bool side_bulk = (a.C & 3) == 0;  // rows of sizes and scores start 16-byte aligned
   for (int pass = 0; pass < 2; ++pass) {
-    if (sc.sel || !(a.stages & (pass == 0 ? kStageScore : kStageSelect))) continue;
+    if ((pass == 1 && sc.sel) || !(a.stages & (pass == 0 ? kStageScore : kStageSelect))) continue;
     const float* src = pass == 0 ? a.kbar : a.vsum;
     const int n = pass == 0 ? sc.n1 : sc.v1 - sc.v0;
     int ready_bg = -1;
     for (int i = 0; i < n; ++i) {
-      const int T = pass == 0 ? sc.kj + i * sc.nk : sc.v0 + i;
+      const int T = pass == 0 ? sc.k0 + i * sc.kstep : sc.v0 + i;
       const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
       const int nrows = min(kTile, a.C - c0);
       const int b = bg / a.Hkv, g = bg - b * a.Hkv;
@@ -1496,8 +1500,8 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     sj = S.sd[stage].s[lane_head<G>(lane)][row];
   };
 
-  // ---- stage 1 (scoring blocks): scores
-  if ((a.stages & kStageScore) && !sc.sel) {
+  // ---- stage 1 (every block): scores
+  if (a.stages & kStageScore) {
     // Every warp stores its scores of tile i - 1 before the barrier of tile
     // i's acquire; thread 0 then hands the count of stored tiles to the
     // signaling warp, which publishes them on the groups' counters.
@@ -1630,7 +1634,7 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
 // ---------------------------------------------------------------------------
 __device__ void signaler(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
   const int lane = threadIdx.x & 31;
-  const int n1 = (!sc.sel && (a.stages & kStageScore)) ? sc.n1 : 0;
+  const int n1 = (a.stages & kStageScore) ? sc.n1 : 0;
   const unsigned per_head = (unsigned)(a.tph + a.r);
   int done1 = 0, ph = 0;
   for (;;) {
@@ -1657,7 +1661,7 @@ __device__ void signaler(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     if (c1 == done1 && pt == ph) break;  // fin: nothing more will come
     fence_gpu();  // every write the consumers made before these requests
     for (int j = done1 + lane; j < c1; j += 32)
-      atomicAdd(a.grp_cnt + (sc.kj + j * sc.nk) / a.tpg, (unsigned)kCW);
+      atomicAdd(a.grp_cnt + (sc.k0 + j * sc.kstep) / a.tpg, (unsigned)kCW);
     if (lane == 0) {
       for (int i = ph; i < pt; ++i) {
         const PubReq q = S.pub[i % kPubSlots];

@@ -188,10 +188,12 @@ WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_cluster
  * inspection of intermediate results.  No device work.  Partials are
  * (m, l, o[d]) triples in log2 units (m is a log2-scaled logit). */
 typedef struct {
-  size_t counters;      /* grid-barrier words (256 B), then i32 [B,Hq] merge
-                           arrival counters and u32 [B,Hq] estimate-ready
-                           marks; zero before the first call, kept
-                           consistent by every call                          */
+  size_t counters;      /* per-call progress counters: a finished-blocks word
+                           (256 B slot), then u32 [B*Hkv] scored tiles,
+                           u32 [B*Hkv] estimate tiles, u32 [B*Hq] merge
+                           arrivals, u32 [B*Hq] selection-ready and
+                           u32 [B*Hq] estimate-ready marks; zero before the
+                           first call; every call leaves them at zero      */
   size_t scores;        /* f32 [B,Hq,C]   s_c = scale q.kbar_c, -inf if empty */
   size_t head_max;      /* f32 [B,Hq]     max_c s_c                           */
   size_t selected;      /* i32 [B,Hq,max(r,1)]  retrieved ids ascending, -1 pad */
@@ -223,8 +225,10 @@ WI_API int wi_decode_workspace_layout(const wi_decode_params *p, int n_clusters,
  * q: bf16 [B,Hq,d]; out: f32 [B,Hq,d]; lse: f32 [B,Hq] or NULL;
  * topk_ids: i32 [B,Hq,r] (ascending ids, -1 padding) or NULL.
  * One persistent cooperative launch of one block per SM runs the three
- * stages below with grid-wide barriers between them (the blocks must be
- * co-resident: the launch fails with WI_ERR_LAUNCH otherwise).  Equivalent to
+ * stages below as one pipeline: blocks wait on per-call counters for exactly
+ * the results they read (a KV group's scores, a head's selection, a group's
+ * estimate pieces), with no grid-wide barrier.  The blocks must be
+ * co-resident: the launch fails with WI_ERR_LAUNCH otherwise.  Equivalent to
  * wi_decode_score, wi_decode_select, wi_decode_attend in order. */
 WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const void *K, const void *V,
                         const wi_index *index, float *out, float *lse, int32_t *topk_ids,
@@ -235,8 +239,8 @@ WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const v
 WI_API int wi_decode_score(const wi_decode_params *p, const void *q, const wi_index *index,
                     void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 2: per query head, the retrieval set T (radix select over the
- * scores; ties to the lower id) with the clusters' sorted rows and sizes, the
+/* Decode stage 2: per query head, the retrieval set T (the r largest scores,
+ * ties to the lower id) with the clusters' sorted rows and sizes, the
  * head's maximum score and the estimate of T (kept with a negative sign); and
  * the estimate of every non-empty cluster (a stream over the value sums).
  * topk_ids may be NULL. */
