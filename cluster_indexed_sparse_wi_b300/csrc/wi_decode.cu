@@ -122,6 +122,12 @@ struct __align__(128) DecSmem {
     int hist[kBins];
     Cand cand;
     float w[kBins];
+    struct {                       // a fast-path selection (ids ascending)
+      unsigned long long comp[kCT];  // candidate composites, then free
+      int c[kCT];                  // cluster ids
+      float s[kCT];                // scores
+      int n[kCT];                  // sizes
+    } kept;
   } u;
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
@@ -368,7 +374,7 @@ __device__ int2 cscan2(int2 v, DecSmem& S, int2* total, int& buf) {
 //   cluster is selected iff k > Kb, or k == Kb and its id <= cb -- and a
 //   compaction pass over all keys writes the selection.
 template <int G>
-__device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
+__device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = bh / a.Hq, h = bh - b * a.Hq, g = h / G;
   const size_t bg = (size_t)b * a.Hkv + g;
@@ -524,7 +530,7 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
           if (w == win)
             pos = ((base[w / 2] + incl[w / 2] - own[w / 2]) >> (16 * (w % 2))) & 0xffffu;
         const uint32_t wsel = window_digits(win);
-        unsigned long long* cand = reinterpret_cast<unsigned long long*>(S.u.hist);
+        unsigned long long* cand = S.u.kept.comp;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const uint32_t k = k0[j];
@@ -570,6 +576,10 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
           rows[p] = rowj;
           cnts[p] = nj;
           if (topk) topk[p] = cid;
+          // kept for the estimate of the selection (estimate_kept)
+          S.u.kept.c[p] = cid;
+          S.u.kept.s[p] = key_float((uint32_t)(mine >> 32));
+          S.u.kept.n[p] = nj;
         }
         for (int i = r_eff + tid; i < rs; i += kCT) {
           ids[i] = -1;
@@ -578,7 +588,7 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
           if (topk && i < r) topk[i] = -1;
         }
         csync();  // the selection is published after this barrier
-        return;
+        return r_eff;
       }
     }
     if (!done) {
@@ -747,6 +757,7 @@ __device__ void select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     }
   }
   csync();  // the selection is published after this barrier
+  return -1;
 }
 
 // The estimate of one head's selected clusters (kept with a negative sign):
@@ -804,6 +815,63 @@ __device__ void estimate_selected(const DecodeArgs& a, DecSmem& S, int bh) {
         o.y += pu * v[u].y;
         o.z += pu * v[u].z;
         o.w += pu * v[u].w;
+      }
+      m = mn;
+    }
+  }
+  combine_write(S, m, l, o, a.neg_part + (size_t)bh * kPartStride, -1.f);
+}
+
+// The same estimate for a fast-path selection, from the ids, scores and sizes
+// select_head kept in shared memory: every value-sum row of the selection is
+// loaded in one round (warp w takes the selected j = w, w + 16, ...).
+template <int G>
+__device__ void estimate_kept(const DecodeArgs& a, DecSmem& S, int bh, int n_sel) {
+  constexpr int kRows = 10;  // rows per warp per round: 160 per round
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+  const size_t bg = (size_t)b * a.Hkv + g;
+  const float4* vs = reinterpret_cast<const float4*>(a.vsum + bg * (size_t)a.C * kD);
+  float m = -INFINITY, l = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = warp; j0 < n_sel; j0 += kCW * kRows) {
+    float4 v[kRows];
+    float x[kRows];
+    int n[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const int j = j0 + u * kCW;
+      n[u] = 0;
+      x[u] = -INFINITY;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < n_sel) {
+        n[u] = S.u.kept.n[j];
+        x[u] = S.u.kept.s[j] * kLog2e;
+        v[u] = __ldg(vs + (size_t)S.u.kept.c[j] * (kD / 4) + lane);
+      }
+    }
+    float mt = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kRows; ++u)
+      if (n[u] > 0) mt = fmaxf(mt, x[u]);
+    if (mt > -INFINITY) {
+      const float mn = fmaxf(m, mt);
+      const float corr = (m > -INFINITY) ? exp2f(m - mn) : 0.f;
+      l *= corr;
+      o.x *= corr;
+      o.y *= corr;
+      o.z *= corr;
+      o.w *= corr;
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        if (n[u] > 0) {
+          const float pu = exp2f(x[u] - mn);
+          l += pu * (float)n[u];
+          o.x += pu * v[u].x;
+          o.y += pu * v[u].y;
+          o.z += pu * v[u].z;
+          o.w += pu * v[u].w;
+        }
       }
       m = mn;
     }
@@ -1532,15 +1600,12 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
       for (int bh = sc.sel0; bh < H; bh += sc.sel_step) {
         const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
         if (!wait_count(a.grp_cnt + (size_t)b * a.Hkv + g, grp_target)) break;
-        select_head<G>(a, S, bh);
+        const int kept = select_head<G>(a, S, bh);
         publish(a.sel_ready + bh, 1u, kPubSet, bh);
-      }
-      // the estimates of this block's selections, published per head
-      if (!bad) {
-        for (int bh = sc.sel0; bh < H; bh += sc.sel_step) {
-          estimate_selected<G>(a, S, bh);
-          publish(a.neg_ready + bh, 1u, kPubSet, bh);
-        }
+        // the estimate of the selection (kept with a negative sign)
+        if (kept >= 0) estimate_kept<G>(a, S, bh, kept);
+        else estimate_selected<G>(a, S, bh);
+        publish(a.neg_ready + bh, 1u, kPubSet, bh);
       }
     } else if (sc.v0 < sc.v1) {
       // (the producer stages a group's tiles once all of its scores are written)
