@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--budget-frac", type=float, default=None,
                     help="retrieval budget as a fraction of clusters (default: workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sdpa", action="store_true",
+                    help="skip the full-attention (torch SDPA) context timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-build-timing", action="store_true")
     return ap.parse_args()
@@ -408,6 +410,34 @@ def main():
     kern_ms = {n: statistics.mean(kev[i][j].elapsed_time(kev[i][j + 1])
                                   for i in range(args.steps)) for j, n in enumerate(names)}
 
+    # ---- context only: full-attention decode over the same K/V with torch SDPA
+    # (every key of the context read once), event-timed like the step
+    sdpa = None
+    if not args.no_sdpa:
+        try:
+            import torch.nn.functional as F
+            q4 = q[:, :, None, :]
+            for _ in range(3):
+                F.scaled_dot_product_attention(q4, K, V, enable_gqa=True)
+            ts = []
+            for _ in range(max(args.steps, 5)):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                F.scaled_dot_product_attention(q4, K, V, enable_gqa=True)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            sdpa_ms = statistics.median(ts)
+            kv_bytes = 2 * K.numel() * K.element_size()
+            sdpa = {"ms": sdpa_ms, "gbs": kv_bytes / (sdpa_ms * 1e-3) / 1e9, "bytes": kv_bytes,
+                    "time_ratio_to_decode_step": sdpa_ms / statistics.mean(step_ms),
+                    "how": "torch scaled_dot_product_attention (bf16, enable_gqa) of the step's "
+                           "queries over all N keys; library kernel, context for the pages' "
+                           "decode speed-up against full attention, not part of the value"}
+        except Exception as e:  # context number only
+            sdpa = {"unavailable": str(e)[:200]}
+
     # ---- e2e through the public API with host buffers (a captured step that
     # copies q from pinned host memory and out/lse back), wall clock per step
     dstep = wl.DecodeStep(dec, K, V)
@@ -485,6 +515,7 @@ def main():
                                   "(score; select + estimate; attend + merge), each a graph "
                                   "replay timed with CUDA events; not the value"},
         "cpu_baseline": cpu,
+        "full_attention_sdpa": sdpa,
         "e2e": {"value": queries / (e2e_mean * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": dstep.h2d_bytes, "d2h_bytes_per_step": dstep.d2h_bytes,
                 "ms_per_step": e2e_mean,
