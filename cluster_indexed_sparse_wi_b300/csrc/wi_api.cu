@@ -15,7 +15,7 @@ using wi::DecodeArgs;
 namespace {
 
 constexpr size_t kStatusBytes = 256;  // status word + reserved
-constexpr size_t kSyncBytes = 256;    // grid-barrier words at the start of the counters region
+constexpr size_t kSyncBytes = 256;    // launch-wide words (blocks finished) at the start of the counters region
 std::atomic<int> g_inject{0};         // wi_debug_inject request
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

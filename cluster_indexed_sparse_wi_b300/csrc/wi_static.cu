@@ -53,8 +53,9 @@ extern "C" int wi_decode_attention_static(const wi_decode_params* p, const void*
   void* ws = nullptr;
   if ((st = scratch_address(&ws)) != WI_OK) return st;
   const cudaStream_t s = (cudaStream_t)stream;
-  // The scratch keeps the previous call's contents: the status word, the grid
-  // barriers and the merge arrival counters must start at zero.
+  // The scratch keeps the previous call's contents (another caller may have
+  // stopped mid-call): the status word and the per-call progress counters
+  // must start at zero.
   char* base = static_cast<char*>(ws);
   if (cudaMemsetAsync(base, 0, lay.counters, s) != cudaSuccess ||
       cudaMemsetAsync(base + lay.counters, 0, (size_t)lay.counter_bytes, s) != cudaSuccess)
