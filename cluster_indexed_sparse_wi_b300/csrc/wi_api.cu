@@ -171,7 +171,7 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   const size_t part = (size_t)wi::kPartStride * 4;
   size_t off = kStatusBytes;
   L->counters = off;
-  L->counter_bytes = (int)align256(kSyncBytes + (2 * groups + 3 * heads) * 4);
+  L->counter_bytes = (int)align256(kSyncBytes + (2 * groups + 5 * heads) * 4);
   off += (size_t)L->counter_bytes;
   L->scores = off;
   off += align256(heads * (size_t)C * 4);
@@ -253,12 +253,16 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
     const size_t heads = (size_t)p->B * p->Hq, groups = (size_t)p->B * p->Hkv;
     unsigned* c = reinterpret_cast<unsigned*>(w + L.counters);
     a->end_cnt = c;
+    a->mq_tail = c + 1;
+    a->mq_head = c + 2;
     a->grp_cnt = c + kSyncBytes / 4;
     a->est_cnt = a->grp_cnt + groups;
     a->head_cnt = a->est_cnt + groups;
     a->sel_ready = a->head_cnt + heads;
     a->neg_ready = a->sel_ready + heads;
-    a->counter_words = (int)(2 * groups + 3 * heads);
+    a->mq_bh = reinterpret_cast<int*>(a->neg_ready + heads);
+    a->mq_ready = a->neg_ready + 2 * heads;
+    a->counter_words = (int)(2 * groups + 5 * heads);
   }
   a->scores = reinterpret_cast<float*>(w + L.scores);
   a->head_max = reinterpret_cast<float*>(w + L.head_max);

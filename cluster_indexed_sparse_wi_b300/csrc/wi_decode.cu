@@ -27,8 +27,9 @@
 //            window) and retrieved-cluster tiles (K/V rows of the
 //            cluster-sorted copies, streamed once the head's selection is
 //            published), exact attention with an online softmax; every
-//            finished piece adds itself to its head's arrival counter and the
-//            block that completes a head merges all of its partials
+//            finished piece adds itself to its head's arrival counter, and a
+//            completed head joins a merge queue from which blocks that have
+//            finished their tiles take heads and merge all of their partials
 //            (log-sum-exp) into out and lse.
 //
 // There is no grid-wide barrier: each consumer of another block's results
@@ -109,7 +110,6 @@ struct PubReq {
   int op, bh, pad;
 };
 constexpr int kPubSlots = 16;
-constexpr int kMergeSlots = 32;  // > kPubSlots + 1: merges queued before the consumers drain them
 
 struct __align__(128) DecSmem {
   unsigned char ring[kStages][kStageBytes];  // bulk-copy destinations (16-byte aligned)
@@ -142,12 +142,8 @@ struct __align__(128) DecSmem {
   int flag;
   int scored;             // stage-1 tiles whose scores every consumer warp has stored
   PubReq pub[kPubSlots];  // requests to the signaling warp (ring)
-  int merge_q[kMergeSlots];  // heads this block merges (ring)
   int pub_tail;           // requests queued (consumer thread 0)
   int pub_head;           // requests done (signaling warp)
-  int merge_tail;         // heads queued for merging (signaling warp)
-  int mt_snap[2];         // merge_tail as seen before tile barriers (by parity of the tile)
-  int mt_final;           // merge_tail once the signaling warp has finished
   int cons_done;          // the consumers queue no more requests
   int sig_done;           // the signaling warp has finished
 };
@@ -1494,8 +1490,6 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
            mbar_wait(smem_addr(&S.full[stage]), (seq / kStages) & 1u, a.status);
       if (ok) S.confirmed = (int)(seq + 1);
       else S.abort = 1;
-      // double-buffered: a warp may still read the previous tile's copy
-      S.mt_snap[seq & 1u] = ld_acquire_cta(&S.merge_tail);
     }
     bad = cany(!ok);
     return !bad;
@@ -1549,17 +1543,6 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
     return wait_count(a.est_cnt + (size_t)b * a.Hkv + g, (unsigned)a.tpg) &&
            wait_count(a.neg_ready + bh, 1u);
-  };
-  // Merge the heads whose last piece this block published, up to mt (queued
-  // by the signaling warp; mt was read by thread 0 before the barrier that
-  // precedes every call).
-  int merges_done = 0;
-  auto drain_merges = [&](int mt) {
-    while (merges_done < mt && !bad) {
-      const int bh = S.merge_q[merges_done % kMergeSlots];
-      ++merges_done;
-      if (merge_ready(bh)) merge_head<G>(a, S, bh);
-    }
   };
   // this lane's size (and, for value-sum tiles, score) of a staged index tile
   auto side_of = [&](int stage, int& n, float& sj) {
@@ -1646,7 +1629,6 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
     for (;;) {
       int stage;
       if (!acquire(stage)) break;
-      drain_merges(S.mt_snap[seq & 1u]);
       const TileInfo t = S.info[stage];
       if (t.kind == kTileEnd) {
         release(stage);
@@ -1672,8 +1654,7 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         if (merge_ready((int)bh)) merge_head<G>(a, S, (int)bh);
     }
   }
-  // No more requests; the signaling warp's last batch may still complete a
-  // head that this block then merges.
+  // No more requests; wait for the signaling warp to publish the last batch.
   if (tid == 0) {
     st_release_cta(&S.cons_done, 1);
     const unsigned long long t0 = global_ns();
@@ -1685,17 +1666,38 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
       }
       __nanosleep(64);
     }
-    S.mt_final = ld_acquire_cta(&S.merge_tail);
   }
   csync();
-  if (a.stages & kStageAttend) drain_merges(S.mt_final);
+  // Merges: a block that has finished its tiles claims slots of the merge
+  // queue, where the signaling warps put every head as its last piece is
+  // published (completion order), and merges them; no block with tiles left
+  // spends time merging.
+  if ((a.stages & kStageAttend) && a.tph + a.r > 0) {
+    const unsigned H = (unsigned)(a.B * a.Hq);
+    for (;;) {
+      if (tid == 0) {
+        int bh = -1;
+        const unsigned slot = *(volatile int*)&S.abort ? H : atomicAdd(a.mq_head, 1u);
+        if (slot < H) {
+          if (count_wait(a.mq_ready + slot, 1u, a.status, &S.abort)) bh = __ldcg(a.mq_bh + slot);
+          else S.abort = 1;
+        }
+        S.flag = bh;
+      }
+      csync();
+      const int bh = S.flag;
+      if (bh < 0) break;
+      if (merge_ready(bh)) merge_head<G>(a, S, bh);  // barriers inside: S.flag is read by then
+      if (bad) break;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
 // signaling warp: publishes the block's results on the grid's counters -- the
 // scored index tiles on the KV groups' counters and the consumers' queued
 // requests -- with one gpu-scope fence per batch, off the consumers' path.
-// A piece that completes its head queues the head's merge for this block.
+// A piece that completes its head puts the head on the launch's merge queue.
 // ---------------------------------------------------------------------------
 __device__ void signaler(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
   const int lane = threadIdx.x & 31;
@@ -1735,10 +1737,13 @@ __device__ void signaler(const DecodeArgs& a, DecSmem& S, const Sched& sc) {
         } else {
           const unsigned old = atomicAdd(q.cnt, q.val);
           if (q.op == kPubPiece && old + q.val == per_head) {
-            fence_gpu();  // the other blocks' pieces before this block's merge reads them
-            const int mt = S.merge_tail;
-            S.merge_q[mt % kMergeSlots] = q.bh;
-            st_release_cta(&S.merge_tail, mt + 1);
+            // the head is complete: queue it for a merging block (the fence
+            // orders every block's pieces, seen through the counter, first)
+            fence_gpu();
+            const unsigned slot = atomicAdd(a.mq_tail, 1u);
+            a.mq_bh[slot] = q.bh;
+            fence_gpu();
+            atomicExch(a.mq_ready + slot, 1u);
           }
         }
       }
@@ -1767,8 +1772,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     S.confirmed = 0;
     S.flag = 0;
     S.scored = 0;
-    S.pub_tail = S.pub_head = S.merge_tail = S.mt_final = 0;
-    S.mt_snap[0] = S.mt_snap[1] = 0;
+    S.pub_tail = S.pub_head = 0;
     S.cons_done = S.sig_done = 0;
   }
   __syncthreads();
@@ -1789,7 +1793,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
   if (S.flag) {
     for (int i = tid; i < a.counter_words; i += kThreads) a.grp_cnt[i] = 0u;
-    if (tid == 0) *a.end_cnt = 0u;
+    if (tid == 0) {
+      *a.mq_tail = 0u;
+      *a.mq_head = 0u;
+      *a.end_cnt = 0u;
+    }
   }
 }
 

@@ -65,12 +65,16 @@ struct DecodeArgs {
   // per-launch progress counters, zero at the start of every launch (the last
   // block to finish resets them)
   unsigned* end_cnt;    // blocks finished
+  unsigned* mq_tail;    // heads queued for merging (in completion order)
+  unsigned* mq_head;    // merge-queue slots claimed
   unsigned* grp_cnt;    // [B*Hkv] scored (index tile, warp) pairs of each KV group
   unsigned* est_cnt;    // [B*Hkv] estimate pieces written for each KV group
   unsigned* head_cnt;   // [B*Hq]  exact-attention units finished for each head
   unsigned* sel_ready;  // [B*Hq]  1 once the head's selection is written
   unsigned* neg_ready;  // [B*Hq]  1 once the estimate of its selection is written
-  int counter_words;    // words from grp_cnt to the end of neg_ready (contiguous)
+  int* mq_bh;           // [B*Hq]  merge queue: the head of each slot
+  unsigned* mq_ready;   // [B*Hq]  1 once the slot's head is written
+  int counter_words;    // words from grp_cnt to the end of mq_ready (contiguous)
   float* scores;        // [B,Hq,C]
   float* head_max;      // [B,Hq]
   int* sel_ids;         // [B,Hq,rs]  retrieved ids ascending, -1 padding (rs = max(r,1))

@@ -188,12 +188,14 @@ WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_cluster
  * inspection of intermediate results.  No device work.  Partials are
  * (m, l, o[d]) triples in log2 units (m is a log2-scaled logit). */
 typedef struct {
-  size_t counters;      /* per-call progress counters: a finished-blocks word
-                           (256 B slot), then u32 [B*Hkv] scored tiles,
-                           u32 [B*Hkv] estimate tiles, u32 [B*Hq] merge
-                           arrivals, u32 [B*Hq] selection-ready and
-                           u32 [B*Hq] estimate-ready marks; zero before the
-                           first call; every call leaves them at zero      */
+  size_t counters;      /* per-call progress counters: finished blocks and
+                           the merge queue's tail and head (256 B slot), then
+                           u32 [B*Hkv] scored tiles, u32 [B*Hkv] estimate
+                           tiles, u32 [B*Hq] merge arrivals, u32 [B*Hq]
+                           selection-ready and u32 [B*Hq] estimate-ready
+                           marks, i32 [B*Hq] merge-queue heads and u32 [B*Hq]
+                           their ready marks; zero before the first call;
+                           every call leaves them at zero                  */
   size_t scores;        /* f32 [B,Hq,C]   s_c = scale q.kbar_c, -inf if empty */
   size_t head_max;      /* f32 [B,Hq]     max_c s_c                           */
   size_t selected;      /* i32 [B,Hq,max(r,1)]  retrieved ids ascending, -1 pad */
