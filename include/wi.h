@@ -65,7 +65,7 @@ typedef enum {
   WI_ERR_CUDA = 8             /* wi_sync_status: the stream reported an error */
 } wi_status;
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define WI_HEAD_DIM 128
 #define WI_MAX_K_PER_SEG 512
 #define WI_MAX_SEG_LEN 16384
