@@ -334,3 +334,74 @@ def test_statistics_invariants_and_stable_order():
     for p in P:
         assert idx["assign"][p] // 10 == p // 200
     assert np.all(idx["assign"][:4] == -1) and np.all(idx["assign"][N - 32:] == -1)
+
+
+# ---------------------------------------------------------------- format and GQA wrapper
+
+def test_bf16_bits_to_f64_every_pattern_matches_torch():
+    # every one of the 65536 bf16 bit patterns except the NaNs, against torch's
+    # own bf16 -> float64 conversion (a library routine, not this code)
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    keep = ~np.isnan(ref)
+    assert keep.sum() == (1 << 16) - 2 * 127
+    with np.errstate(invalid="ignore"):  # the NaN patterns are dropped below
+        got = wi.bf16_bits_to_f64(bits)
+    np.testing.assert_array_equal(got[keep], ref[keep])
+    # signed zeros and infinities keep their sign
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0])
+    assert got[0x7F80] == np.inf and got[0xFF80] == -np.inf
+
+
+def _gqa_case(seed=30, B=2, Hq=8, Hkv=2, N=600, d=32, sink=3, window=20, seg=128, k=12):
+    rng = np.random.default_rng(seed)
+    K = bf16_vals(rng, (B, Hkv, N, d))
+    V = bf16_vals(rng, (B, Hkv, N, d))
+    q = bf16_vals(rng, (B, Hq, d), 0.6)
+    idx = wi.build_index(K, V, sink, window, seg, k, 2)
+    return K, V, q, idx, dict(sink=sink, window=window)
+
+
+def test_decode_wrapper_full_budget_is_torch_gqa_attention():
+    # With a budget covering every cluster each head is exact attention over its
+    # KV head; torch's SDPA with enable_gqa maps query head h to KV head
+    # h // (Hq / Hkv), so a wrong head mapping in the wrapper fails here.
+    K, V, q, idx, z = _gqa_case()
+    B, Hq, d = q.shape
+    C = idx["n_clusters"]
+    scale = 0.21
+    res = wi.decode(q, K, V, idx, z["sink"], z["window"], C, scale)
+    qt = torch.from_numpy(q)[:, :, None, :]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, torch.from_numpy(K), torch.from_numpy(V), scale=scale, enable_gqa=True)[:, :, 0]
+    np.testing.assert_allclose(res["out"], ref.numpy(), rtol=1e-11, atol=1e-13)
+    logits = scale * np.einsum("bhd,bhnd->bhn", q, np.repeat(K, Hq // K.shape[1], axis=1))
+    lse = torch.logsumexp(torch.from_numpy(logits), dim=-1).numpy()
+    np.testing.assert_allclose(res["lse"], lse, rtol=0, atol=1e-11)
+
+
+def test_decode_wrapper_budgeted_rows_and_head_subset():
+    # Below full budget: every head of a group uses its own KV head's index,
+    # and a KV head's data never leaks into another group's heads (swapping the
+    # two KV heads' data swaps the groups' results); heads outside the
+    # requested subset stay NaN.
+    K, V, q, idx, z = _gqa_case(seed=31)
+    r = 5
+    full = wi.decode(q, K, V, idx, z["sink"], z["window"], r, 0.2)
+    assert np.isfinite(full["out"]).all() and np.isfinite(full["lse"]).all()
+    swap = lambda a: a[:, ::-1].copy()
+    idx_s = {key: (val if key == "n_clusters" else swap(val)) for key, val in idx.items()}
+    q_s = np.concatenate([q[:, 4:], q[:, :4]], axis=1)
+    res_s = wi.decode(q_s, swap(K), swap(V), idx_s, z["sink"], z["window"], r, 0.2)
+    np.testing.assert_array_equal(res_s["out"][:, 4:], full["out"][:, :4])
+    np.testing.assert_array_equal(res_s["out"][:, :4], full["out"][:, 4:])
+    # a query head of group 1 attends over KV head 1 only: replacing KV head 0
+    # changes nothing for it
+    K2 = K.copy()
+    K2[:, 0] = K2[:, 0][:, ::-1]
+    idx2 = wi.build_index(K2, V, z["sink"], z["window"], 128, 12, 2)
+    part = wi.decode(q, K2, V, idx2, z["sink"], z["window"], r, 0.2, heads=[(1, 6), (0, 5)])
+    np.testing.assert_array_equal(part["out"][1, 6], full["out"][1, 6])
+    np.testing.assert_array_equal(part["out"][0, 5], full["out"][0, 5])
+    assert np.isnan(part["out"][0, 0]).all() and np.isnan(part["lse"][1, 1])
+    assert set(part["selected"]) == {(1, 6), (0, 5)}
