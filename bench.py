@@ -50,6 +50,8 @@ def parse():
                     help="skip the full-attention (torch SDPA) context timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-build-timing", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the 1M-context and batch-16 decode workloads")
     return ap.parse_args()
 
 
@@ -138,7 +140,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("wi_decode.cu", "wi_device.cuh", "wi_internal.h", "wi_assign.cu", "wi_build.cu"):
+    for name in ("wi_decode.cu", "wi_device.cuh", "wi_internal.h", "wi_assign.cu", "wi_build.cu",
+                 "wi_api.cu"):
         with open(os.path.join(ROOT, "cluster_indexed_sparse_wi_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -286,9 +289,165 @@ def workload_config(w, r):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
             "clusters_per_head": w.n_clusters, "seg_len": w.seg_len, "k_per_seg": w.k_per_seg,
             "kmeans_iters": w.iters, "sink": w.sink, "window": w.window, "r": r,
-            "l2": "flushed between timed steps (256 MiB write)",
-            "step": "decode (score; select + estimate; attend + merge) over an index built in the "
-                    "same run; build timed separately under 'build'"}
+            "l2": L2_HOW,
+            "step": "decode (score + estimate of every cluster; select; attend + merge) over an "
+                    "index built in the same run; build timed separately under 'build'"}
+
+
+L2_HOW = ("flushed before every timed step, outside the events: a 256 MiB write, then a "
+          "512 MiB read that evicts the lines the write left dirty, so that no input is "
+          "L2-resident and the step does not pay the flush's write-back; the same steps "
+          "after the write alone are reported as ms_per_step_write_flush")
+
+
+class L2Flush:
+    """Evicts every L2 line between timed steps: a 256 MiB write (the
+    classic flush) followed by a 512 MiB read."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)  # 512 MiB
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+        self.k = 0
+
+    def write_only(self):
+        self.k += 1
+        self.w.fill_(self.k & 0xFF)
+
+    def __call__(self):
+        import torch
+        self.write_only()
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
+def decode_bytes(w, ix, topk, r):
+    """Algorithmic bytes of one decode step: centroid keys and value sums with
+    the sizes, once; steady K/V; retrieved K/V once per (sequence, KV head,
+    cluster)."""
+    C = w.n_clusters
+    kbar = w.B * w.Hkv * C * (w.d * 4 + 4)
+    vsum = w.B * w.Hkv * C * (w.d * 4 + 4)
+    steady = w.B * w.Hkv * (w.sink + w.window) * w.d * 2 * 2
+    retr = retrieved_unique_bytes(topk[..., :r].contiguous(), ix.size, w.Hq // w.Hkv) if r else 0
+    return {"centroid_keys": kbar, "value_sums_sizes": vsum, "steady_kv": steady,
+            "retrieved_kv_unique": retr}
+
+
+def timed_steps(fn, flush, steps, stream):
+    """Event time of `steps` calls of fn, each after flush() (outside the
+    events); returns the per-step milliseconds."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def measure_workload(w, r, dev, args, pk, flush, rank=0, want_cpu=False, label=None):
+    """Build the index of workload w on the GPU, then time the fused decode
+    call (CUDA-graph replays) and its end-to-end host step; returns one
+    result dict with its own roofline, clocks and e2e."""
+    import torch
+    import cluster_indexed_sparse_wi_b300 as wl
+    from workloads import generate
+    t0 = time.perf_counter()
+    wr = replica_workload(w, rank)
+    g_np = generate(wr)
+    t_gen = time.perf_counter() - t0
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    K, V, q = up(g_np["K"]), up(g_np["V"]), up(g_np["q"])
+    cfg = wl.IndexConfig(w.B, w.Hkv, w.N, w.sink, w.window, w.seg_len, w.k_per_seg, w.iters)
+    ix = wl.WaveIndex(cfg, dev)
+    ix.build(K, V)
+    torch.cuda.synchronize()
+    assert ix.status() == 0
+    stream = torch.cuda.current_stream()
+    dec = wl.Decoder(ix, w.Hq, r)
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        dec(q, K, V, with_topk=False)
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    g_step = dec.capture(q, K, V)
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        g_step.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid_str(dev))
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    step_ms = timed_steps(g_step.replay, flush, args.steps, stream)
+    wall = time.perf_counter() - wall0
+    wflush_ms = timed_steps(g_step.replay, flush.write_only, args.steps, stream)
+    clocks = sampler.stop()
+    assert dec.status() == 0
+    # e2e through the public API with host buffers
+    dstep = wl.DecodeStep(dec, K, V)
+    q_src = q.cpu()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush()
+        torch.cuda.synchronize()
+        a0 = time.perf_counter()
+        out_h, _ = dstep(q_src)
+        a1 = time.perf_counter()
+        if i >= args.warmup:
+            e2e_ms.append((a1 - a0) * 1e3)
+    assert torch.isfinite(out_h).all() and dec.status() == 0
+    dec(q, K, V, with_topk=True)
+    torch.cuda.synchronize()
+    by = decode_bytes(w, ix, dec.topk, r)
+    step_bytes = sum(by.values())
+    ms = statistics.mean(step_ms)
+    e2e_mean = statistics.mean(e2e_ms)
+    hbm_peak = float(pk["hbm_gbs"])
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    res = {
+        "workload": label or w.name, "r": r, "ms_per_step": ms,
+        "ms_per_step_median": statistics.median(step_ms),
+        "ms_per_step_write_flush": statistics.mean(wflush_ms),
+        "value": w.B / (ms * 1e-3), "unit": UNIT,
+        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": gbs / hbm_peak,
+                     "algorithmic_bytes_per_launch": step_bytes, "launch_ms": ms,
+                     "frac_of_8tbs": gbs / NOMINAL_HBM_GBS},
+        "bytes": by,
+        "e2e": {"value": w.B / (e2e_mean * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": dstep.h2d_bytes, "d2h_bytes_per_step": dstep.d2h_bytes,
+                "ms_per_step": e2e_mean},
+        "clocks": clocks, "gpu_launches": args.steps, "wall_s_timed": wall,
+        "setup_seconds": {"generate": t_gen},
+    }
+    if want_cpu and rank == 0 and not args.no_cpu_baseline:
+        index_np = {
+            "size": ix.size[0, 0].cpu().numpy().astype(np.int64),
+            "centroid_key": ix.centroid_key[0, 0].double().cpu().numpy(),
+            "value_sum": ix.value_sum[0, 0].double().cpu().numpy(),
+            "perm": ix.perm[0, 0].cpu().numpy().astype(np.int64),
+            "offset": ix.offset[0, 0].cpu().numpy().astype(np.int64),
+        }
+        val, desc, _ = oracle_decode_sample(w, g_np, index_np, r, args.cpu_seconds / 2)
+        res["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": blas_threads(),
+                               "kind": "oracle", "sample": desc, "host_cpus": os.cpu_count()}
+    ctx = {"w": w, "g_np": g_np, "K": K, "V": V, "q": q, "ix": ix, "dec": dec, "dstep": dstep,
+           "step_ms": step_ms}
+    return res, ctx
+
+
+def gpu_uuid_str(dev):
+    import torch
+    u = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    return "GPU-" + str(u) if u else ""
 
 
 # ----------------------------------------------------------------------------
@@ -305,7 +464,6 @@ def main():
     import torch
     import torch.distributed as dist
     import cluster_indexed_sparse_wi_b300 as wl
-    from cluster_indexed_sparse_wi_b300 import _lib
 
     ws, rank, local = dist_env()
     if ws > 1:
@@ -313,31 +471,20 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pk, pk_kind = peaks()
-
-    # per-rank replica: own sequences (weak scaling), no data-path collective
-    t0 = time.perf_counter()
-    wr = replica_workload(w, rank)
-    g_np = generate(wr)
-    t_gen = time.perf_counter() - t0
-
-    def up(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    K, V, q = up(g_np["K"]), up(g_np["V"]), up(g_np["q"])
-    cfg = wl.IndexConfig(w.B, w.Hkv, w.N, w.sink, w.window, w.seg_len, w.k_per_seg, w.iters)
-    ix = wl.WaveIndex(cfg, dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
+    # ---- the headline workload: decode (value), its stages, e2e, oracle
+    res, ctx = measure_workload(w, r, dev, args, pk, flush, rank, want_cpu=False)
+    K, V, q, ix, dec, g_np = ctx["K"], ctx["V"], ctx["q"], ctx["ix"], ctx["dec"], ctx["g_np"]
+    C = w.n_clusters
+
     # ---- build (rows a1-a4), timed on its own
-    ix.build(K, V)
-    torch.cuda.synchronize()
-    assert ix.status() == 0
     build = None
     if not args.no_build_timing:
         bt = []
         for _ in range(3):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             ix.build(K, V)
@@ -351,67 +498,31 @@ def main():
                  "assign_tflop": flops * 1e-12,
                  "assign_tflops_over_whole_build": flops / (build_ms * 1e-3) * 1e-12,
                  "launches": 2 + 3 * w.iters + 1}
-    assert ix.status() == 0
+        assert ix.status() == 0
 
-    dec = wl.Decoder(ix, w.Hq, r)
-
-    def step():
-        dec(q, K, V, with_topk=False)
-
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    assert dec.status() == 0
-    # Steps are replayed as CUDA graphs so that the host runs ahead of the GPU
-    # and the events time the GPU work alone.
-    g_step = dec.capture(q, K, V)
+    # ---- the same step as three stage-only launches (reported, not the value)
+    names = ["score", "select", "attend"]
     g_stage = [wl.capture_graph(fn, dev) for fn in (
         lambda: dec.score(q), lambda: dec.select(), lambda: dec.attend(q, K, V))]
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        g_step.replay()
-    torch.cuda.synchronize()
-
-    # ---- timed region 1: the fused decode call (value)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    gpu_uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
-    sampler = ClockSampler("GPU-" + str(gpu_uuid) if gpu_uuid else "")
-    sampler.start()
-    time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        g_step.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-
-    # ---- timed region 2 (reported, not the value): the same step as three
-    # stage-only launches of the decode kernel
-    names = ["score", "select", "attend"]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         e = kev[i]
         e[0].record(stream)
-        for j, g in enumerate(g_stage):
-            g.replay()
+        for j, gs in enumerate(g_stage):
+            gs.replay()
             e[j + 1].record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
     assert dec.status() == 0
     kern_ms = {n: statistics.mean(kev[i][j].elapsed_time(kev[i][j + 1])
                                   for i in range(args.steps)) for j, n in enumerate(names)}
+    by = res["bytes"]
+    kern_bytes = {"score": by["centroid_keys"] + by["value_sums_sizes"],
+                  "select": w.B * w.Hq * C * 4,
+                  "attend": by["steady_kv"] + by["retrieved_kv_unique"]}
+    stage_gbs = {n: kern_bytes[n] / (kern_ms[n] * 1e-3) / 1e9 for n in names}
 
     # ---- context only: full-attention decode over the same K/V with torch SDPA
-    # (every key of the context read once), event-timed like the step
     sdpa = None
     if not args.no_sdpa:
         try:
@@ -419,73 +530,17 @@ def main():
             q4 = q[:, :, None, :]
             for _ in range(3):
                 F.scaled_dot_product_attention(q4, K, V, enable_gqa=True)
-            ts = []
-            for _ in range(max(args.steps, 5)):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                F.scaled_dot_product_attention(q4, K, V, enable_gqa=True)
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1))
+            ts = timed_steps(lambda: F.scaled_dot_product_attention(q4, K, V, enable_gqa=True),
+                             flush, max(args.steps, 5), stream)
             sdpa_ms = statistics.median(ts)
             kv_bytes = 2 * K.numel() * K.element_size()
             sdpa = {"ms": sdpa_ms, "gbs": kv_bytes / (sdpa_ms * 1e-3) / 1e9, "bytes": kv_bytes,
-                    "time_ratio_to_decode_step": sdpa_ms / statistics.mean(step_ms),
+                    "time_ratio_to_decode_step": sdpa_ms / res["ms_per_step"],
                     "how": "torch scaled_dot_product_attention (bf16, enable_gqa) of the step's "
                            "queries over all N keys; library kernel, context for the pages' "
                            "decode speed-up against full attention, not part of the value"}
         except Exception as e:  # context number only
             sdpa = {"unavailable": str(e)[:200]}
-
-    # ---- e2e through the public API with host buffers (a captured step that
-    # copies q from pinned host memory and out/lse back), wall clock per step
-    dstep = wl.DecodeStep(dec, K, V)
-    q_src = q.cpu()
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        out_h, lse_h = dstep(q_src)
-        t1 = time.perf_counter()
-        if i >= args.warmup:
-            e2e_ms.append((t1 - t0) * 1e3)
-    assert torch.isfinite(out_h).all() and dec.status() == 0
-
-    # ---- bytes
-    dec(q, K, V, with_topk=True)
-    torch.cuda.synchronize()
-    C = cfg.n_clusters
-    n_size = ix.size
-    kbar_bytes = w.B * w.Hkv * C * (w.d * 4 + 4)
-    vsum_bytes = w.B * w.Hkv * C * (w.d * 4 + 4)
-    steady_bytes = w.B * w.Hkv * (w.sink + w.window) * w.d * 2 * 2
-    retr_bytes = retrieved_unique_bytes(dec.topk[..., :r].contiguous(), n_size, w.Hq // w.Hkv)
-    step_bytes = kbar_bytes + vsum_bytes + steady_bytes + retr_bytes
-    # the select stage also streams the value sums (estimate of every cluster)
-    kern_bytes = {"score": kbar_bytes, "select": vsum_bytes, "attend": steady_bytes + retr_bytes}
-
-    ms = statistics.mean(step_ms)
-    e2e_mean = statistics.mean(e2e_ms)
-    if ws > 1:
-        ms, e2e_mean = max_over_ranks([ms, e2e_mean], dist, dev)
-    queries = w.B * ws
-    value = queries / (ms * 1e-3)
-
-    # The step is one launch of decode_kernel (the graph holds nothing else), so
-    # the kernel's launch duration is the event time of a step.
-    hbm_peak = float(pk["hbm_gbs"])
-    step_gbs = step_bytes / (ms * 1e-3) / 1e9
-    roofline = {"kernel": "decode_kernel", "bound": "hbm", "achieved": step_gbs, "peak": hbm_peak,
-                "unit": "GB/s", "frac": step_gbs / hbm_peak,
-                "traffic": recorded_traffic("decode_kernel", w.name),
-                "algorithmic_bytes_per_launch": step_bytes,
-                "launch_ms": ms,
-                "peak_source": pk_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"
-                if pk_kind == "measured" else "fallback 6.4 TB/s"}
-    stage_gbs = {n: (kern_bytes[n] / (kern_ms[n] * 1e-3) / 1e9 if kern_bytes[n] else 0.0)
-                 for n in names}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -499,25 +554,58 @@ def main():
         val, desc, _ = oracle_decode_sample(w, g_np, index_np, r, args.cpu_seconds)
         cpu = {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": desc, "host_cpus": os.cpu_count()}
+    del ctx, K, V, q, ix, dec, g_np
+    torch.cuda.empty_cache()
 
+    # ---- the other decode workloads (their own roofline, clocks, e2e)
+    sweep = []
+    if not args.no_sweep and ws == 1:
+        for name, fracs, want_cpu in (("llama3_8b_1m_b1", (None,), True),
+                                      ("llama3_8b_128k_b16", (0.01, 0.02, 0.03), False)):
+            wx = WORKLOADS[name]
+            for k, fr in enumerate(fracs):
+                rx = retrieval_budget(wx, fr) if fr else wx.r
+                label = name if fr is None else "%s@%g%%" % (name, fr * 100)
+                try:
+                    rx_res, cx = measure_workload(wx, rx, dev, args, pk, flush, rank,
+                                                  want_cpu=want_cpu, label=label)
+                    sweep.append(rx_res)
+                    del cx
+                    torch.cuda.empty_cache()
+                except Exception as e:  # report, keep the headline
+                    sweep.append({"workload": label, "error": str(e)[:300]})
+
+    ms = res["ms_per_step"]
+    e2e_mean = res["e2e"]["ms_per_step"]
+    if ws > 1:
+        ms, e2e_mean = max_over_ranks([ms, e2e_mean], dist, dev)
+    queries = w.B * ws
+    value = queries / (ms * 1e-3)
+    roofline = dict(res["roofline"])
+    roofline["traffic"] = recorded_traffic("decode_kernel", w.name)
+    roofline["peak_source"] = (pk_kind + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                               if pk_kind == "measured" else "fallback 6.4 TB/s")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(w, r),
         "roofline": roofline,
-        "hbm": {"algorithmic_bytes_per_step": step_bytes, "achieved_gbs": step_gbs,
-                "frac_of_measured": step_gbs / hbm_peak, "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
-                "bytes": {"centroid_keys": kbar_bytes, "value_sums_sizes": vsum_bytes,
-                          "steady_kv": steady_bytes, "retrieved_kv_unique": retr_bytes}},
+        "ms_per_step_write_flush": res["ms_per_step_write_flush"],
+        "hbm": {"algorithmic_bytes_per_step": roofline["algorithmic_bytes_per_launch"],
+                "achieved_gbs": roofline["achieved"], "frac_of_measured": roofline["frac"],
+                "frac_of_8tbs": roofline["frac_of_8tbs"], "bytes": res["bytes"],
+                "frac_of_measured_write_flush": roofline["algorithmic_bytes_per_launch"] /
+                (res["ms_per_step_write_flush"] * 1e-3) / 1e9 / roofline["peak"]},
         "stage_launches": {"ms": kern_ms, "algorithmic_bytes": kern_bytes, "gbs": stage_gbs,
                            "how": "the step as three stage-only launches of decode_kernel "
-                                  "(score; select + estimate; attend + merge), each a graph "
+                                  "(score + estimate; select; attend + merge), each a graph "
                                   "replay timed with CUDA events; not the value"},
         "cpu_baseline": cpu,
         "full_attention_sdpa": sdpa,
         "e2e": {"value": queries / (e2e_mean * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": dstep.h2d_bytes, "d2h_bytes_per_step": dstep.d2h_bytes,
+                "h2d_bytes_per_step": res["e2e"]["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": res["e2e"]["d2h_bytes_per_step"],
                 "ms_per_step": e2e_mean,
                 "how": "DecodeStep graph: H2D q (pinned), decode_kernel, D2H out+lse (pinned), "
                        "host waits; wall clock per step (q copied into the pinned buffer "
@@ -525,11 +613,12 @@ def main():
         "gpu_launches": args.steps,
         "timing": "CUDA events around CUDA-graph replays of the decode call; L2 flushed "
                   "before every step outside the events",
-        "clocks": clocks,
+        "clocks": res["clocks"],
         "build": build,
         "full_pass_ms": (build["ms"] + ms) if build else None,
-        "wall_s_timed_region_1": wall,
-        "setup_seconds": {"generate": t_gen},
+        "sweep": sweep,
+        "wall_s_timed_region_1": res["wall_s_timed"],
+        "setup_seconds": res["setup_seconds"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

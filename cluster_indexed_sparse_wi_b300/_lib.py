@@ -33,7 +33,7 @@ SYMBOLS = [
     "wi_index_sizes", "wi_build_workspace_bytes", "wi_build_index", "wi_build_init",
     "wi_kmeans_assign", "wi_kmeans_update", "wi_build_finalize", "wi_decode_workspace_bytes",
     "wi_decode_workspace_layout", "wi_decode_attention", "wi_decode_score", "wi_decode_select",
-    "wi_decode_attend", "wi_decode_attention_static", "wi_sync_status", "wi_status_string", "wi_debug_inject",
+    "wi_decode_attend", "wi_decode_attention_static", "wi_decode_static_status", "wi_sync_status", "wi_status_string", "wi_debug_inject",
     "wi_version",
 ]
 
@@ -66,7 +66,7 @@ class IndexStruct(ctypes.Structure):
 class DecodeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("counters", "scores", "head_max", "selected", "sel_rows", "sel_counts",
-                 "partials", "total")] + [
+                 "sel_prefix", "sel_scores", "head_tokens", "partials", "total")] + [
         (n, ctypes.c_int) for n in ("counter_bytes", "max_blocks", "reserved0", "reserved1")]
 
 
@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
         "wi_decode_select": (i, [dp, ip, vp, vp, sz, vp]),
         "wi_decode_attend": (i, [dp, vp, vp, vp, ip, vp, vp, vp, sz, vp]),
         "wi_decode_attention_static": (i, [dp, vp, vp, vp, ip, vp, vp, vp, vp]),
+        "wi_decode_static_status": (i, [vp, P(i)]),
         "wi_sync_status": (i, [vp, vp, P(i)]),
         "wi_status_string": (ctypes.c_char_p, [i]),
         "wi_debug_inject": (i, [i]),

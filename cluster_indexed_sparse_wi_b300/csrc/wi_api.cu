@@ -15,7 +15,7 @@ using wi::DecodeArgs;
 namespace {
 
 constexpr size_t kStatusBytes = 256;  // status word + reserved
-constexpr size_t kSyncBytes = 256;    // launch-wide words (blocks finished) at the start of the counters region
+constexpr size_t kSyncBytes = 256;    // launch-wide words (blocks finished, selections published) at the start of the counters region
 std::atomic<int> g_inject{0};         // wi_debug_inject request
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -160,6 +160,37 @@ int check_decode(const wi_decode_params* p, int C) {
   return WI_OK;
 }
 
+// Index tiles, steady tiles and chunking of a decode over C clusters on nb
+// blocks (the kernel's static schedule).
+struct DecodeShape {
+  int tpg, tph, nt, Q, nchunks, rounds;
+};
+DecodeShape decode_shape(const wi_decode_params* p, int C, int nb) {
+  DecodeShape d;
+  d.tpg = (C + wi::kDecodeTile - 1) / wi::kDecodeTile;
+  d.tph = (p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile;
+  d.nt = p->B * p->Hkv * d.tpg;
+  // chunks of at most kChunkMax tiles, about equal, in whole rounds of nb
+  const long long per_round = (long long)nb * wi::kChunkMax;
+  int rounds = (int)((d.nt + per_round - 1) / per_round);
+  if (rounds < 1) rounds = 1;
+  d.Q = (int)((d.nt + (long long)nb * rounds - 1) / ((long long)nb * rounds));
+  if (d.Q < 1) d.Q = 1;
+  d.nchunks = (d.nt + d.Q - 1) / d.Q;
+  d.rounds = (d.nchunks + nb - 1) / nb;
+  return d;
+}
+
+// Chunks are at most kChunkMax tiles and number at most nb per round, so
+// nchunks <= nt / kChunkMax + nb: a bound that does not depend on the device.
+size_t est_slots(const wi_decode_params* p, int C) {
+  const size_t tpg = (size_t)(C + wi::kDecodeTile - 1) / wi::kDecodeTile;
+  const size_t nt = (size_t)p->B * p->Hkv * tpg;
+  size_t nch = nt / wi::kChunkMax + wi::kMaxBlocks + 1;
+  if (nch > nt) nch = nt;
+  return nch + (size_t)p->B * p->Hkv;
+}
+
 int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   const int st = check_decode(p, C);
   if (st != WI_OK) return st;
@@ -169,9 +200,10 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   const size_t G = (size_t)(p->Hq / p->Hkv);
   const size_t rs = p->r > 0 ? (size_t)p->r : 1;
   const size_t part = (size_t)wi::kPartStride * 4;
+  const size_t tph = (size_t)(p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile;
   size_t off = kStatusBytes;
   L->counters = off;
-  L->counter_bytes = (int)align256(kSyncBytes + (2 * groups + 5 * heads) * 4);
+  L->counter_bytes = (int)align256(kSyncBytes + (groups + heads) * 4);
   off += (size_t)L->counter_bytes;
   L->scores = off;
   off += align256(heads * (size_t)C * 4);
@@ -183,23 +215,60 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   off += align256(heads * rs * 4);
   L->sel_counts = off;
   off += align256(heads * rs * 4);
+  L->sel_prefix = off;
+  off += align256(heads * rs * 4);
+  L->sel_scores = off;
+  off += align256(heads * rs * 4);
+  L->head_tokens = off;
+  off += align256(heads * 4);
   L->partials = off;
-  off += align256((wi::kMaxBlocks + groups) * G * part);  // estimate of every cluster
-  off += align256((wi::kMaxBlocks + heads) * part);       // steady pieces
-  off += align256((wi::kMaxBlocks + heads) * part);       // retrieved pieces
-  off += align256(heads * part);                          // selected clusters' estimate
+  off += align256(est_slots(p, C) * G * part);         // estimate pieces
+  off += align256(groups * tph * G * part);            // steady pieces
+  off += align256((wi::kMaxBlocks + heads) * part);    // retrieval pieces
   L->total = off;
   L->max_blocks = wi::kMaxBlocks;
   return WI_OK;
 }
 
-// Cost of one per-head selection in units of one centroid-key tile (64 rows).
-double selection_weight(int C) { return 8.0 + C / 1024.0; }
+// Streamed-work equivalent of one per-head selection, in 4 KB units (the
+// scores and sizes it reads and the passes over them).
+unsigned selection_units(int C) { return 16u + (unsigned)(C / 1024); }
+
+}  // namespace
+
+namespace wi {
+
+int decode_precheck(const wi_decode_params* p, const void* q, const void* K, const void* V,
+                    const wi_index* ix, const float* out) {
+  if (p == nullptr || ix == nullptr) return WI_ERR_INVALID_ARG;
+  int st = check_decode(p, ix->n_clusters);
+  if (st != WI_OK) return st;
+  if (ix->B != p->B || ix->Hkv != p->Hkv || ix->N != p->N || ix->d != p->d ||
+      ix->sink != p->sink || ix->window != p->window)
+    return WI_ERR_INDEX_MISMATCH;
+  const bool no_idx = p->N - p->sink - p->window == 0;  // sorted arrays may be NULL then
+  const void* req[] = {ix->centroid_key, ix->value_sum, ix->size, ix->offset,
+                       ix->k_sorted, ix->v_sorted};
+  for (int i = 0; i < 6; ++i) {
+    if (req[i] == nullptr && !(no_idx && i >= 4)) return WI_ERR_INVALID_ARG;
+    if (!aligned(req[i], 16)) return WI_ERR_ALIGNMENT;
+  }
+  if (q == nullptr || K == nullptr || V == nullptr || out == nullptr) return WI_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16)) return WI_ERR_ALIGNMENT;
+  const long long n_tiles = (long long)p->B * p->Hkv *
+                            ((ix->n_clusters + wi::kDecodeTile - 1) / wi::kDecodeTile);
+  if (n_tiles >= (1LL << 31) || (long long)p->B * p->Hq >= (1LL << 31)) return WI_ERR_UNSUPPORTED;
+  return device_ok();
+}
+
+}  // namespace wi
+
+namespace {
 
 int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, const void* V,
                      const wi_index* ix, void* ws, size_t ws_bytes, DecodeArgs* a,
-                     bool need_kv) {
-  if (ix == nullptr || ws == nullptr) return WI_ERR_INVALID_ARG;
+                     bool need_q, bool need_kv) {
+  if (p == nullptr || ix == nullptr || ws == nullptr) return WI_ERR_INVALID_ARG;
   wi_decode_layout L;
   int st = decode_layout(p, ix->n_clusters, &L);
   if (st != WI_OK) return st;
@@ -215,14 +284,17 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
     if (req[i] == nullptr && !(no_idx && i >= 4)) return WI_ERR_INVALID_ARG;
     if (!aligned(req[i], 16)) return WI_ERR_ALIGNMENT;
   }
+  if (need_q) {
+    if (q == nullptr) return WI_ERR_INVALID_ARG;
+    if (!aligned(q, 16)) return WI_ERR_ALIGNMENT;
+  }
   if (need_kv) {
-    if (q == nullptr || K == nullptr || V == nullptr) return WI_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16)) return WI_ERR_ALIGNMENT;
+    if (K == nullptr || V == nullptr) return WI_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(V, 16)) return WI_ERR_ALIGNMENT;
   }
   const int C = ix->n_clusters;
-  const int tpg = (C + wi::kDecodeTile - 1) / wi::kDecodeTile;
-  const long long n_tiles = (long long)p->B * p->Hkv * tpg;
-  if (n_tiles >= (1LL << 31)) return WI_ERR_UNSUPPORTED;
+  const long long n_tiles = (long long)p->B * p->Hkv * ((C + wi::kDecodeTile - 1) / wi::kDecodeTile);
+  if (n_tiles >= (1LL << 31) || (long long)p->B * p->Hq >= (1LL << 31)) return WI_ERR_UNSUPPORTED;
   if ((st = device_ok()) != WI_OK) return st;
   int nb = 0;
   if (wi::decode_blocks(&nb) != cudaSuccess || nb < 2) return WI_ERR_LAUNCH;
@@ -249,57 +321,48 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->ksorted = static_cast<const uint16_t*>(ix->k_sorted);
   a->vsorted = static_cast<const uint16_t*>(ix->v_sorted);
   a->status = reinterpret_cast<int*>(w);
+  const size_t heads = (size_t)p->B * p->Hq, groups = (size_t)p->B * p->Hkv;
   {
-    const size_t heads = (size_t)p->B * p->Hq, groups = (size_t)p->B * p->Hkv;
     unsigned* c = reinterpret_cast<unsigned*>(w + L.counters);
     a->end_cnt = c;
-    a->mq_tail = c + 1;
-    a->mq_head = c + 2;
+    a->sel_done = c + 1;
     a->grp_cnt = c + kSyncBytes / 4;
-    a->est_cnt = a->grp_cnt + groups;
-    a->head_cnt = a->est_cnt + groups;
-    a->sel_ready = a->head_cnt + heads;
-    a->neg_ready = a->sel_ready + heads;
-    a->mq_bh = reinterpret_cast<int*>(a->neg_ready + heads);
-    a->mq_ready = a->neg_ready + 2 * heads;
-    a->counter_words = (int)(2 * groups + 5 * heads);
+    a->head_cnt = a->grp_cnt + groups;
+    a->counter_words = (int)(groups + heads);
   }
   a->scores = reinterpret_cast<float*>(w + L.scores);
   a->head_max = reinterpret_cast<float*>(w + L.head_max);
   a->sel_ids = reinterpret_cast<int*>(w + L.selected);
   a->sel_rows = reinterpret_cast<int*>(w + L.sel_rows);
   a->sel_cnts = reinterpret_cast<int*>(w + L.sel_counts);
-  const size_t heads = (size_t)p->B * p->Hq, groups = (size_t)p->B * p->Hkv;
+  a->sel_pre = reinterpret_cast<int*>(w + L.sel_prefix);
+  a->sel_sc = reinterpret_cast<float*>(w + L.sel_scores);
+  a->head_tok = reinterpret_cast<int*>(w + L.head_tokens);
   const size_t part = (size_t)wi::kPartStride * 4;
+  const DecodeShape d = decode_shape(p, C, nb);
   size_t off = L.partials;
   a->est_part = reinterpret_cast<float*>(w + off);
-  off += align256((wi::kMaxBlocks + groups) * (size_t)a->G * part);
+  off += align256(est_slots(p, C) * (size_t)a->G * part);
   a->std_part = reinterpret_cast<float*>(w + off);
-  off += align256((wi::kMaxBlocks + heads) * part);
+  off += align256(groups * (size_t)d.tph * (size_t)a->G * part);
   a->ret_part = reinterpret_cast<float*>(w + off);
-  off += align256((wi::kMaxBlocks + heads) * part);
-  a->neg_part = reinterpret_cast<float*>(w + off);
   a->nb = nb;
-  a->tpg = tpg;
-  a->tph = (p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile;
-  // Blocks [0, nsel) select (heads dealt round robin); the others stream the
-  // value-sum tiles (every block scores centroid-key tiles).  The split
-  // minimises the larger of the two loads, a selection costing about
-  // selection_weight() tiles.
-  const long long H = (long long)p->B * p->Hq;
-  const double wsel = selection_weight(C);
-  int best = 1;
-  double best_cost = 1e300;
-  for (int ns = 1; ns <= nb - 1 && ns <= H; ++ns) {
-    const double sel = (double)((H + ns - 1) / ns) * wsel;
-    const double idx = (double)((n_tiles + (nb - ns) - 1) / (nb - ns));
-    const double cost = sel > idx ? sel : idx;
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = ns;
-    }
-  }
-  a->nsel = best;
+  a->tpg = d.tpg;
+  a->tph = d.tph;
+  a->nt = d.nt;
+  a->Q = d.Q;
+  a->nchunks = d.nchunks;
+  a->rounds = d.rounds;
+  // static work of every block (4 KB units): its index tiles (centroid keys
+  // and value sums, 64 KB per tile), steady tiles (32 KB) and selections
+  const unsigned su = selection_units(C);
+  for (int b = 0; b < nb; ++b) a->static_w[b] = 0u;
+  for (int j = 0; j < a->nchunks; ++j) a->static_w[j % nb] += 16u * (unsigned)wi::chunk_tiles(*a, j);
+  const long long nst = (long long)groups * d.tph;
+  for (long long t = 0; t < nst; ++t) a->static_w[wi::steady_block(*a, t)] += 8u;
+  for (size_t bh = 0; bh < heads; ++bh) a->static_w[wi::sel_block(*a, (int)bh)] += su;
+  a->static_units = 0;
+  for (int b = 0; b < nb; ++b) a->static_units += a->static_w[b];
   return WI_OK;
 }
 
@@ -307,12 +370,9 @@ int run_decode(const wi_decode_params* p, const void* q, const void* K, const vo
                const wi_index* index, float* out, float* lse, int32_t* topk_ids, void* workspace,
                size_t workspace_bytes, wi_stream_t stream, int stages, bool need_q, bool need_kv) {
   if ((stages & wi::kStageAttend) && out == nullptr) return WI_ERR_INVALID_ARG;
-  if (need_q && !need_kv) {
-    if (q == nullptr) return WI_ERR_INVALID_ARG;
-    if (!aligned(q, 16)) return WI_ERR_ALIGNMENT;
-  }
   DecodeArgs a;
-  const int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_kv);
+  const int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_q,
+                                  need_kv);
   if (st != WI_OK) return st;
   a.stages = stages;
   a.fused = stages == (wi::kStageScore | wi::kStageSelect | wi::kStageAttend) ? 1 : 0;

@@ -43,9 +43,13 @@ struct BuildArgs {
 constexpr int kMaxBlocks = 256;
 constexpr int kPartStride = 2 + 128;  // (m, l, o[128]) per partial
 constexpr int kDecodeTile = 64;       // index rows / tokens per staging tile
+constexpr int kChunkMax = 16;         // index tiles per chunk
+// Static work per block is counted in units of 4 KB of streamed bytes, i.e.
+// 8 tokens of K and V (512 bytes per token).
+constexpr int kTokPerUnit = 8;
 
-// Which decode stages one launch runs (wi_decode_attention runs all three,
-// with grid-wide barriers between them).
+// Which decode stages one launch runs (wi_decode_attention runs all three in
+// one launch whose blocks wait on each other's results).
 enum : int { kStageScore = 1, kStageSelect = 2, kStageAttend = 4 };
 
 struct DecodeArgs {
@@ -62,41 +66,77 @@ struct DecodeArgs {
   const uint16_t* vsorted;
   // workspace regions
   int* status;
-  // per-launch progress counters, zero at the start of every launch (the last
-  // block to finish resets them)
+  // per-launch progress counters: zero when a launch starts; the last block
+  // to finish clears them again
   unsigned* end_cnt;    // blocks finished
-  unsigned* mq_tail;    // heads queued for merging (in completion order)
-  unsigned* mq_head;    // merge-queue slots claimed
-  unsigned* grp_cnt;    // [B*Hkv] scored (index tile, warp) pairs of each KV group
-  unsigned* est_cnt;    // [B*Hkv] estimate pieces written for each KV group
-  unsigned* head_cnt;   // [B*Hq]  exact-attention units finished for each head
-  unsigned* sel_ready;  // [B*Hq]  1 once the head's selection is written
-  unsigned* neg_ready;  // [B*Hq]  1 once the estimate of its selection is written
-  int* mq_bh;           // [B*Hq]  merge queue: the head of each slot
-  unsigned* mq_ready;   // [B*Hq]  1 once the slot's head is written
-  int counter_words;    // words from grp_cnt to the end of mq_ready (contiguous)
-  float* scores;        // [B,Hq,C]
+  unsigned* sel_done;   // heads whose selection is published
+  unsigned* grp_cnt;    // [B*Hkv] index tiles scored per KV group
+  unsigned* head_cnt;   // [B*Hq]  partials published per query head
+  int counter_words;    // words from grp_cnt to the end of head_cnt (contiguous)
+  float* scores;        // [B,Hq,C]   s_c (f32), -inf for empty clusters
   float* head_max;      // [B,Hq]
   int* sel_ids;         // [B,Hq,rs]  retrieved ids ascending, -1 padding (rs = max(r,1))
   int* sel_rows;        // [B,Hq,rs]  first sorted row of each retrieved cluster
-  int* sel_cnts;        // [B,Hq,rs]  members of each retrieved cluster (0 = padding)
-  float* est_part;      // [kMaxBlocks + B*Hkv][G][kPartStride]
-  float* std_part;      // [kMaxBlocks + B*Hq][kPartStride]
-  float* ret_part;      // [kMaxBlocks + B*Hq][kPartStride]
-  float* neg_part;      // [B*Hq][kPartStride]
+  int* sel_cnts;        // [B,Hq,rs]  members of each (0 = padding)
+  int* sel_pre;         // [B,Hq,rs]  members of the clusters before it (token offset)
+  float* sel_sc;        // [B,Hq,rs]  its score s_c
+  int* head_tok;        // [B,Hq]     retrieved tokens of the head
+  float* est_part;      // [(nchunks + B*Hkv) * G][kPartStride]
+  float* std_part;      // [B*Hkv*tph * G][kPartStride]
+  float* ret_part;      // [(nb + B*Hq)][kPartStride]
   // schedule (identical in every block)
   int nb;               // grid size
-  int nsel;             // blocks [0, nsel) select; the others score
   int stages;           // kStage* mask
   int fused;            // the stages run in one launch and wait on each other
   int tpg;              // index tiles per KV group: ceil(C / 64)
-  int tph;              // steady tiles per query head: ceil((sink + window) / 64)
+  int tph;              // steady tiles per KV group: ceil((sink + window) / 64)
+  int nt;               // index tiles: B * Hkv * tpg
+  int Q;                // index tiles per chunk (<= kChunkMax)
+  int nchunks;          // ceil(nt / Q); chunk j is taken by block j % nb in round j / nb
+  int rounds;           // ceil(nchunks / nb)
   int inject;           // test hook: every block skips the copies of its first tile
+  long long static_units;         // sum of static_w
+  unsigned static_w[kMaxBlocks];  // static work of each block, 4 KB units
   // outputs
   int* topk_out;        // [B,Hq,r] or null
   float* out;           // [B,Hq,128]
   float* lse;           // [B,Hq] or null
 };
+
+// ---- the static schedule, shared by the host (work estimates) and the kernel
+// Chunk j holds index tiles [j*Q, min((j+1)*Q, nt)).
+__host__ __device__ inline int chunk_tiles(const DecodeArgs& a, int j) {
+  const int lo = j * a.Q, hi = lo + a.Q < a.nt ? lo + a.Q : a.nt;
+  return hi > lo ? hi - lo : 0;
+}
+__host__ __device__ inline int first_chunk(const DecodeArgs& a, int bg) {
+  return (int)((long long)bg * a.tpg / a.Q);
+}
+__host__ __device__ inline int last_chunk(const DecodeArgs& a, int bg) {
+  return (int)(((long long)bg * a.tpg + a.tpg - 1) / a.Q);
+}
+// Head bh (b*Hq + h) of KV group bg = bh / G is selected by block
+// (last_chunk(bg) - bh % G) mod nb, after that block's centroid-key tiles of
+// round last_chunk(bg) / nb: a selection only waits on chunks of its own or
+// earlier rounds.
+__host__ __device__ inline int sel_block(const DecodeArgs& a, int bh) {
+  const int x = (last_chunk(a, bh / a.G) - bh % a.G) % a.nb;
+  return x < 0 ? x + a.nb : x;
+}
+__host__ __device__ inline int sel_round(const DecodeArgs& a, int bh) {
+  return last_chunk(a, bh / a.G) / a.nb;
+}
+// Steady tile t (of B*Hkv*tph) is taken by block nb - 1 - t % nb.
+__host__ __device__ inline int steady_block(const DecodeArgs& a, long long t) {
+  return a.nb - 1 - (int)(t % a.nb);
+}
+// Head bh is merged by block bh % nb.
+__host__ __device__ inline int merge_block(const DecodeArgs& a, int bh) { return bh % a.nb; }
+
+// Host checks of a decode call that need no workspace (parameters, index,
+// pointers, device); wi_api.cu.
+int decode_precheck(const wi_decode_params* p, const void* q, const void* K, const void* V,
+                    const wi_index* ix, const float* out);
 
 // decode launcher (wi_decode.cu): one persistent launch of the stages in
 // a.stages on a.nb blocks.

@@ -45,20 +45,30 @@ int scratch_address(void** out) {
 extern "C" int wi_decode_attention_static(const wi_decode_params* p, const void* q, const void* K,
                                           const void* V, const wi_index* index, float* out,
                                           float* lse, int32_t* topk_ids, wi_stream_t stream) {
-  if (p == nullptr || index == nullptr) return WI_ERR_INVALID_ARG;
-  wi_decode_layout lay;
-  int st = wi_decode_workspace_layout(p, index->n_clusters, &lay);
+  // every host check first: a rejected call queues nothing on the stream and
+  // leaves the scratch (and its status word) untouched
+  int st = wi::decode_precheck(p, q, K, V, index, out);
   if (st != WI_OK) return st;
+  wi_decode_layout lay;
+  if ((st = wi_decode_workspace_layout(p, index->n_clusters, &lay)) != WI_OK) return st;
   if (lay.total > kScratchBytes) return WI_ERR_WORKSPACE;  // beyond the fixed scratch
   void* ws = nullptr;
   if ((st = scratch_address(&ws)) != WI_OK) return st;
   const cudaStream_t s = (cudaStream_t)stream;
   // The scratch keeps the previous call's contents (another caller may have
-  // stopped mid-call): the status word and the per-call progress counters
-  // must start at zero.
+  // stopped mid-call): the per-call progress counters must start at zero.
+  // The status word is left alone, so that an error of an earlier call stays
+  // readable through wi_decode_static_status until it is read.
   char* base = static_cast<char*>(ws);
-  if (cudaMemsetAsync(base, 0, lay.counters, s) != cudaSuccess ||
-      cudaMemsetAsync(base + lay.counters, 0, (size_t)lay.counter_bytes, s) != cudaSuccess)
+  if (cudaMemsetAsync(base + lay.counters, 0, (size_t)lay.counter_bytes, s) != cudaSuccess)
     return WI_ERR_LAUNCH;
   return wi_decode_attention(p, q, K, V, index, out, lse, topk_ids, ws, kScratchBytes, stream);
+}
+
+extern "C" int wi_decode_static_status(wi_stream_t stream, int* device_status) {
+  if (device_status == nullptr) return WI_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const int st = scratch_address(&ws);
+  if (st != WI_OK) return st;
+  return wi_sync_status(ws, stream, device_status);
 }

@@ -188,21 +188,22 @@ WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_cluster
  * inspection of intermediate results.  No device work.  Partials are
  * (m, l, o[d]) triples in log2 units (m is a log2-scaled logit). */
 typedef struct {
-  size_t counters;      /* per-call progress counters: finished blocks and
-                           the merge queue's tail and head (256 B slot), then
-                           u32 [B*Hkv] scored tiles, u32 [B*Hkv] estimate
-                           tiles, u32 [B*Hq] merge arrivals, u32 [B*Hq]
-                           selection-ready and u32 [B*Hq] estimate-ready
-                           marks, i32 [B*Hq] merge-queue heads and u32 [B*Hq]
-                           their ready marks; zero before the first call;
+  size_t counters;      /* per-call progress counters: launch-wide words
+                           (blocks finished, selections published; 256 B),
+                           then u32 [B*Hkv] scored index tiles and u32 [B*Hq]
+                           published partials; zero before the first call;
                            every call leaves them at zero                  */
   size_t scores;        /* f32 [B,Hq,C]   s_c = scale q.kbar_c, -inf if empty */
   size_t head_max;      /* f32 [B,Hq]     max_c s_c                           */
   size_t selected;      /* i32 [B,Hq,max(r,1)]  retrieved ids ascending, -1 pad */
   size_t sel_rows;      /* i32 [B,Hq,max(r,1)]  first k_sorted row of each      */
   size_t sel_counts;    /* i32 [B,Hq,max(r,1)]  its size n_c (0 for padding)     */
-  size_t partials;      /* f32 partials: estimate pieces, steady pieces,
-                           retrieved pieces, selected clusters' estimate       */
+  size_t sel_prefix;    /* i32 [B,Hq,max(r,1)]  retrieved tokens before it       */
+  size_t sel_scores;    /* f32 [B,Hq,max(r,1)]  its score s_c (-inf padding)     */
+  size_t head_tokens;   /* i32 [B,Hq]     retrieved tokens of the head           */
+  size_t partials;      /* f32 partials: estimate pieces (per chunk of index
+                           tiles and query head), steady pieces (per steady
+                           tile and query head), retrieval pieces            */
   size_t total;
   int counter_bytes;    /* bytes of the counters region                        */
   int max_blocks;       /* blocks the partial buffers are sized for            */
@@ -223,35 +224,37 @@ WI_API int wi_decode_workspace_layout(const wi_decode_params *p, int n_clusters,
  *   out  = (sum_S e^{l_i - M} v_i + sum_E e^{s_c - M} value_sum_c) / L,
  *   lse  = M + ln L  (log-sum-exp merge of the three zones).
  * The E sums are formed as (all non-empty clusters) minus (clusters in T), in
- * f32; this reorders the arithmetic only.
+ * f32: every member i of a cluster c in T enters with the weight
+ * e^{l_i} - e^{s_c}; this reorders the arithmetic only.
  * q: bf16 [B,Hq,d]; out: f32 [B,Hq,d]; lse: f32 [B,Hq] or NULL;
  * topk_ids: i32 [B,Hq,r] (ascending ids, -1 padding) or NULL.
  * One persistent cooperative launch of one block per SM runs the three
  * stages below as one pipeline: blocks wait on per-call counters for exactly
- * the results they read (a KV group's scores, a head's selection, a group's
- * estimate pieces), with no grid-wide barrier.  The blocks must be
+ * the results they read (a KV group's scores, the published selections, a
+ * head's partials), with no grid-wide barrier.  The blocks must be
  * co-resident: the launch fails with WI_ERR_LAUNCH otherwise.  Equivalent to
  * wi_decode_score, wi_decode_select, wi_decode_attend in order. */
 WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const void *K, const void *V,
                         const wi_index *index, float *out, float *lse, int32_t *topk_ids,
                         void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 1: cluster scores s into the workspace (a stream over the
- * centroid keys). */
+/* Decode stage 1: one stream over the centroid keys and the value sums:
+ * the cluster scores s into the workspace, and the estimate of every
+ * non-empty cluster, (m, l = sum n_c e^{s_c - m}, o = sum e^{s_c - m}
+ * value_sum_c), as partials. */
 WI_API int wi_decode_score(const wi_decode_params *p, const void *q, const wi_index *index,
                     void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
 /* Decode stage 2: per query head, the retrieval set T (the r largest scores,
- * ties to the lower id) with the clusters' sorted rows and sizes, the
- * head's maximum score and the estimate of T (kept with a negative sign); and
- * the estimate of every non-empty cluster (a stream over the value sums).
- * topk_ids may be NULL. */
+ * ties to the lower id) with the clusters' sorted rows, sizes, token offsets
+ * and scores, and the head's maximum score.  topk_ids may be NULL. */
 WI_API int wi_decode_select(const wi_decode_params *p, const wi_index *index, int32_t *topk_ids,
                      void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
-/* Decode stage 3: exact attention over the steady zone and the retrieved
- * clusters, and the log-sum-exp merge of every partial into out and lse (lse
- * may be NULL). */
+/* Decode stage 3: exact attention over the steady zone and over the members
+ * of T, each member i of cluster c weighted e^{l_i} - e^{s_c} (its exact term
+ * minus its share of the cluster's estimate), and the log-sum-exp merge of
+ * every partial into out and lse (lse may be NULL). */
 WI_API int wi_decode_attend(const wi_decode_params *p, const void *q, const void *K, const void *V,
                      const wi_index *index, float *out, float *lse, void *workspace,
                      size_t workspace_bytes, wi_stream_t stream);
@@ -276,11 +279,20 @@ WI_API int wi_decode_attend(const wi_decode_params *p, const void *q, const void
  *    overlap on the GPU race and corrupt each other's results.  Each call
  *    clears the parts that must start at zero; the rest keeps the previous
  *    call's contents.
- *  - Device-side errors (a bounded wait that ran out) land in the shared
- *    scratch and are not reported through wi_sync_status. */
+ *  - Argument errors are found before anything is enqueued.  Device-side
+ *    errors (a bounded wait that ran out) are recorded in the scratch's status
+ *    word, which keeps the first error until wi_decode_static_status reads
+ *    and clears it. */
 WI_API int wi_decode_attention_static(const wi_decode_params *p, const void *q, const void *K,
                                const void *V, const wi_index *index, float *out, float *lse,
                                int32_t *topk_ids, wi_stream_t stream);
+
+/* The device status of wi_decode_attention_static on the current device:
+ * synchronise `stream`, then read and clear the status word of the fixed
+ * scratch into *device_status (host), as wi_sync_status does for a
+ * workspace.  Like the decode, its first call on a device looks the
+ * scratch's address up there. */
+WI_API int wi_decode_static_status(wi_stream_t stream, int *device_status);
 
 /* Synchronise `stream`, then read and clear the device status word at the
  * start of `workspace` into *device_status (host).  Returns WI_OK, or

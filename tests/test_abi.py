@@ -120,14 +120,23 @@ def test_decode_layout(L):
     assert lib.wi_decode_workspace_layout(ctypes.byref(dp(L)), 256, ctypes.byref(lay)) == 0
     assert lay.total == lib.wi_decode_workspace_bytes(ctypes.byref(dp(L)), 256)
     regions = [lay.counters, lay.scores, lay.head_max, lay.selected, lay.sel_rows,
-               lay.sel_counts, lay.partials, lay.total]
+               lay.sel_counts, lay.sel_prefix, lay.sel_scores, lay.head_tokens, lay.partials,
+               lay.total]
     assert regions == sorted(regions) and all(r % 256 == 0 for r in regions)
     assert lay.head_max - lay.scores >= 8 * 256 * 4
-    assert lay.scores - lay.counters == lay.counter_bytes >= 256 + 8 * 8
-    assert lay.sel_rows - lay.selected >= 8 * 8 * 4
-    # partial buffers: per block and KV group / query head, (m, l, o[128]) each
+    # launch-wide words, then one scored-tile counter per KV group and one
+    # partial counter per query head
+    assert lay.scores - lay.counters == lay.counter_bytes >= 256 + (2 + 8) * 4
+    for lo, hi in ((lay.selected, lay.sel_rows), (lay.sel_rows, lay.sel_counts),
+                   (lay.sel_counts, lay.sel_prefix), (lay.sel_prefix, lay.sel_scores),
+                   (lay.sel_scores, lay.head_tokens)):
+        assert hi - lo >= 8 * 8 * 4
+    # partials, (m, l, o[128]) each: estimate pieces (at most one per index
+    # tile and KV group, G heads each), steady pieces (2 tiles per KV group, G
+    # heads each), retrieval pieces (one per block and query head)
     part = (2 + 128) * 4
-    assert lay.total - lay.partials >= part * ((lay.max_blocks + 2) * 4 + 2 * (lay.max_blocks + 8) + 8)
+    tiles = 2 * (256 // 64)
+    assert lay.total - lay.partials >= part * ((tiles + 2) * 4 + 2 * 2 * 4 + lay.max_blocks + 8)
 
 
 @pytest.mark.parametrize("kw,code", [
