@@ -232,7 +232,7 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
 
 // Streamed-work equivalent of one per-head selection, in 4 KB units (the
 // scores and sizes it reads and the passes over them).
-unsigned selection_units(int C) { return 16u + (unsigned)(C / 1024); }
+unsigned selection_units(int C) { return 8u + (unsigned)(C / 128); }
 
 }  // namespace
 
@@ -295,6 +295,9 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   const int C = ix->n_clusters;
   const long long n_tiles = (long long)p->B * p->Hkv * ((C + wi::kDecodeTile - 1) / wi::kDecodeTile);
   if (n_tiles >= (1LL << 31) || (long long)p->B * p->Hq >= (1LL << 31)) return WI_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->Hkv * ((p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile) >=
+      (1LL << 31))
+    return WI_ERR_UNSUPPORTED;
   if ((st = device_ok()) != WI_OK) return st;
   int nb = 0;
   if (wi::decode_blocks(&nb) != cudaSuccess || nb < 2) return WI_ERR_LAUNCH;
@@ -358,8 +361,8 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   const unsigned su = selection_units(C);
   for (int b = 0; b < nb; ++b) a->static_w[b] = 0u;
   for (int j = 0; j < a->nchunks; ++j) a->static_w[j % nb] += 16u * (unsigned)wi::chunk_tiles(*a, j);
-  const long long nst = (long long)groups * d.tph;
-  for (long long t = 0; t < nst; ++t) a->static_w[wi::steady_block(*a, t)] += 8u;
+  const int nst = (int)groups * d.tph;
+  for (int t = 0; t < nst; ++t) a->static_w[wi::steady_block(*a, t)] += 8u;
   for (size_t bh = 0; bh < heads; ++bh) a->static_w[wi::sel_block(*a, (int)bh)] += su;
   a->static_units = 0;
   for (int b = 0; b < nb; ++b) a->static_units += a->static_w[b];

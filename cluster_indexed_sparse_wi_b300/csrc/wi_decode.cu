@@ -72,8 +72,8 @@ constexpr int kTile = kDecodeTile;             // index rows or tokens per tile
 constexpr uint32_t kStageBytes = kTile * 512;  // 64 f32 rows, or 64 K + 64 V bf16 rows
 constexpr int kQSlotBytes = 8 * kD * 2;        // up to 8 bf16 query rows
 constexpr int kSlots = kStages + 1;            // retrieval pieces in flight (see consumers)
-constexpr int kBins = 2048;                    // selection histogram
-constexpr int kCand = 512;                     // selection candidates ranked exactly
+constexpr int kBins = 1024;                    // selection histogram
+constexpr int kCand = 256;                     // selection candidates ranked exactly
 constexpr int kSelChunk = kCT * 16;            // keys per register chunk (16 per thread)
 constexpr int kPubSlots = 32;
 static_assert(kSlots >= kStages + 1, "a warp may run kStages tiles ahead of the slowest");
@@ -127,6 +127,7 @@ struct __align__(128) DecSmem {
       float l[kCW][4];
     } comb;
     struct {
+      uint32_t key[16][kCT];  // keys of the first 8192 clusters: id 16 t + j at [j][t]
       int hist[kBins];
       unsigned long long cand[kCand];
       int ncand;
@@ -144,6 +145,7 @@ struct __align__(128) DecSmem {
   unsigned long long empty[kStages];
   TileInfo info[kStages];
   int bnd[kMaxBlocks + 1];  // token start of every block's retrieval range
+  unsigned static_w[kMaxBlocks];  // copy of the blocks' static work
   unsigned slot_cnt[kSlots];
   int2 scan[2][kCW];
   uint32_t red_u[4][kCW];
@@ -163,6 +165,7 @@ static_assert(offsetof(DecSmem, a) % 16 == 0, "float4 alignment");
 static_assert(offsetof(DecSmem, u) % 16 == 0, "float4 alignment");
 static_assert(offsetof(DecSmem, full) % 8 == 0, "mbarrier alignment");
 static_assert(sizeof(WarpPart) % 16 == 0, "float4 alignment");
+static_assert(sizeof(DecSmem) <= 227 * 1024, "dynamic shared memory per block");
 
 // ---------------------------------------------------------------------------
 // small helpers
@@ -370,17 +373,24 @@ __device__ void combine_write(DecSmem& S, const float (&m)[NH], const float (&l)
 // ---------------------------------------------------------------------------
 // selection of one query head (all 512 consumers)
 // ---------------------------------------------------------------------------
-// T = the r_eff = min(r, non-empty) largest scores, ties to the lower id.  Keys
-// (order-preserving images of the scores, 0 = empty cluster) are held in
-// registers for the first 8192 clusters (16 consecutive ids per thread) and
-// re-read for the rest.  The r_eff-th key is found by histograms over the key
-// range: 2048 equal bins between the smallest and largest key; the bin
-// holding the boundary is narrowed the same way until it holds at most 512
-// keys, which are then ranked exactly by (key desc, id asc), or until it
-// holds one key value, whose lowest ids are taken.  A cluster is then selected
-// iff its key k and id c satisfy k > Kb, or k == Kb and c <= cb.  A last pass
-// writes the selection in id order with the clusters' sorted rows, sizes,
-// token offsets and scores.  Returns the number selected.
+// T = the r_eff = min(r, non-empty) largest scores, ties to the lower id.
+// Keys are order-preserving images of the scores (0 = empty cluster).  The
+// keys of the first 8192 clusters are kept in shared memory (thread t holds
+// ids 16 t .. 16 t + 15); the rest are re-read from the scores at every pass.
+//   1. count, smallest and largest key;
+//   2. a histogram of 1024 bins linear in the score between the smallest and
+//      largest score (monotone in the score, so few keys share a bin) gives
+//      the bin holding the r_eff-th largest key;
+//   3. that bin's keys (normally a few) are ranked exactly by (key desc, id
+//      asc); the r_eff-th overall gives the threshold (Kb, cb): a cluster is
+//      selected iff its key k and id c satisfy k > Kb, or k == Kb and c <= cb.
+//      A bin of more than 256 keys is narrowed by histograms of its key range
+//      until it holds at most 256 keys, or a single key value whose lowest
+//      ids are then taken;
+//   4. the selected ids are written in id order; then every selected
+//      cluster's size, first sorted row and score are loaded in one round and
+//      a scan of the sizes gives the token offsets.
+// Returns the number selected.
 __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bg = bh / a.G;
@@ -392,70 +402,78 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const bool vec = (C & 3) == 0;  // rows of scores start on 16-byte boundaries
   int buf = 0;
 
-  auto load16 = [&](int ch, uint32_t(&k)[16]) {
+  // keys of chunk ch for this thread, in groups of four: f(key, id)
+  auto chunk_keys = [&](int ch, auto&& f) {
     const int c0 = ch * kSelChunk + tid * 16;
     if (vec && c0 + 16 <= C) {
       const float4* p = reinterpret_cast<const float4*>(sc + c0);
+      float4 v[4];  // all four loads in flight before any key is used
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __ldcg(p + j);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float4 f = __ldcg(p + j);
-        k[4 * j] = score_key(f.x);
-        k[4 * j + 1] = score_key(f.y);
-        k[4 * j + 2] = score_key(f.z);
-        k[4 * j + 3] = score_key(f.w);
+        f(score_key(v[j].x), c0 + 4 * j);
+        f(score_key(v[j].y), c0 + 4 * j + 1);
+        f(score_key(v[j].z), c0 + 4 * j + 2);
+        f(score_key(v[j].w), c0 + 4 * j + 3);
       }
     } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) k[j] = (c0 + j < C) ? score_key(__ldcg(sc + c0 + j)) : 0u;
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) f((c0 + j < C) ? score_key(__ldcg(sc + c0 + j)) : 0u, c0 + j);
     }
   };
-  uint32_t k0[16];
-  load16(0, k0);
-  // f(key, id) over every key
+  // f(key, id) over every key: chunk 0 from shared memory
   auto visit = [&](auto&& f) {
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) f(S.u.sel.key[j][tid], tid * 16 + j);
+    for (int ch = 1; ch < nch; ++ch) chunk_keys(ch, f);
+  };
+  // block sum and key extrema (one barrier)
+  auto block_count_range = [&](int& cnt, uint32_t& kmx, uint32_t& kmn) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) f(k0[j], tid * 16 + j);
-    for (int ch = 1; ch < nch; ++ch) {
-      uint32_t kk[16];
-      load16(ch, kk);
+    for (int o = 16; o > 0; o >>= 1) {
+      cnt += __shfl_xor_sync(kFull, cnt, o);
+      kmx = max(kmx, __shfl_xor_sync(kFull, kmx, o));
+      kmn = min(kmn, __shfl_xor_sync(kFull, kmn, o));
+    }
+    int2* sh = S.scan[buf];
+    uint32_t(*ru)[kCW] = buf ? &S.red_u[2] : &S.red_u[0];
+    buf ^= 1;
+    if (lane == 0) {
+      sh[warp] = make_int2(cnt, 0);
+      ru[0][warp] = kmx;
+      ru[1][warp] = kmn;
+    }
+    csync();
+    cnt = 0;
+    kmx = 0u;
+    kmn = 0xffffffffu;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) f(kk[j], ch * kSelChunk + tid * 16 + j);
+    for (int w = 0; w < kCW; ++w) {
+      cnt += sh[w].x;
+      kmx = max(kmx, ru[0][w]);
+      kmn = min(kmn, ru[1][w]);
     }
   };
 
-  // non-empty count and key range
+  // 1. keys of the first chunk into shared memory; count and key range
   int valid = 0;
   uint32_t kmax = 0u, kmin = 0xffffffffu;
-  visit([&](uint32_t k, int) {
+  auto tally = [&](uint32_t k, int) {
     valid += (int)(k != 0u);
     kmax = max(kmax, k);
     kmin = min(kmin, k != 0u ? k : 0xffffffffu);
-  });
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    valid += __shfl_xor_sync(kFull, valid, o);
-    kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
-    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
-  }
+  };
   {
-    int2* sh = S.scan[buf];
-    buf ^= 1;
-    if (lane == 0) {
-      sh[warp] = make_int2(valid, 0);
-      S.red_u[0][warp] = kmax;
-      S.red_u[1][warp] = kmin;
-    }
-    csync();
-    valid = 0;
-    kmax = 0u;
-    kmin = 0xffffffffu;
-#pragma unroll
-    for (int w = 0; w < kCW; ++w) {
-      valid += sh[w].x;
-      kmax = max(kmax, S.red_u[0][w]);
-      kmin = min(kmin, S.red_u[1][w]);
-    }
+    int j = 0;
+    chunk_keys(0, [&](uint32_t k, int id) {
+      S.u.sel.key[id - tid * 16][tid] = k;
+      tally(k, id);
+      ++j;
+    });
   }
+  for (int ch = 1; ch < nch; ++ch) chunk_keys(ch, tally);
+  block_count_range(valid, kmax, kmin);
   const int r_eff = min(r, valid);
   if (tid == 0) a.head_max[bh] = valid > 0 ? key_float(kmax) : -INFINITY;
 
@@ -464,122 +482,147 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   int cb = -1;
   if (r_eff > 0 && r_eff == valid) {
     Kb = 0u;  // every non-empty cluster
+    cb = INT_MAX;
   } else if (r_eff > 0) {
-    uint32_t lo = kmin, span = kmax - kmin;  // keys in [lo, lo + span]
-    int need = r_eff;
-    for (int iter = 0; iter < 8; ++iter) {
-      int shift = 0;
-      while ((span >> shift) >= (uint32_t)kBins) ++shift;
-      for (int i = tid; i < kBins; i += kCT) S.u.sel.hist[i] = 0;
-      csync();
-      {
-        const uint32_t l0 = lo, sp = span;
-        const int sh = shift;
-        visit([&](uint32_t k, int) {
-          if (k != 0u && k - l0 <= sp) atomicAdd(&S.u.sel.hist[(k - l0) >> sh], 1);
-        });
-      }
-      csync();
-      // thread t owns the 4 bins kBins-4t-4 .. kBins-4t-1 (from the top)
-      const int b_hi = kBins - 4 * tid;
-      int cnt4[4], own = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        cnt4[i] = S.u.sel.hist[b_hi - 1 - i];
-        own += cnt4[i];
-      }
+    // 2. score-linear histogram: the bin of the r_eff-th largest key
+    const float smin = key_float(kmin), smax = key_float(kmax);
+    const float inv = (smax > smin) ? (float)kBins / (smax - smin) : 0.f;
+    auto bin_of = [&](uint32_t k) {
+      const float x = (key_float(k) - smin) * inv;
+      return x < (float)(kBins - 1) ? (int)x : kBins - 1;
+    };
+    for (int i = tid; i < kBins; i += kCT) S.u.sel.hist[i] = 0;
+    if (tid == 0) S.u.sel.ncand = 0;
+    csync();
+    visit([&](uint32_t k, int) {
+      if (k != 0u) atomicAdd(&S.u.sel.hist[bin_of(k)], 1);
+    });
+    csync();
+    // boundary bin: thread t owns the 2 bins kBins-2t-2 .. kBins-2t-1 (from the top)
+    auto boundary = [&](int need_in) {
+      const int b_hi = kBins - 2 * tid;
+      const int c1 = S.u.sel.hist[b_hi - 1], c2 = S.u.sel.hist[b_hi - 2];
       int2 tot;
-      const int above0 = cscan2(make_int2(own, 0), S, &tot, buf).x;
-      if (own > 0 && above0 < need && need <= above0 + own) {
-        int acc = above0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (acc < need && need <= acc + cnt4[i]) {
-            S.u.sel.res[0] = b_hi - 1 - i;
-            S.u.sel.res[1] = acc;
-            S.u.sel.res[2] = cnt4[i];
-          }
-          acc += cnt4[i];
-        }
+      const int above0 = cscan2(make_int2(c1 + c2, 0), S, &tot, buf).x;
+      if (above0 < need_in && need_in <= above0 + c1) {
+        S.u.sel.res[0] = b_hi - 1;
+        S.u.sel.res[1] = above0;
+        S.u.sel.res[2] = c1;
+      } else if (above0 + c1 < need_in && need_in <= above0 + c1 + c2) {
+        S.u.sel.res[0] = b_hi - 2;
+        S.u.sel.res[1] = above0 + c1;
+        S.u.sel.res[2] = c2;
       }
-      if (tid == 0) S.u.sel.ncand = 0;
       csync();
-      const int bstar = S.u.sel.res[0], above = S.u.sel.res[1], nbin = S.u.sel.res[2];
-      need -= above;
-      const uint32_t bin_lo = lo + ((uint32_t)bstar << shift);
-      const uint32_t bin_span = min(span - ((uint32_t)bstar << shift),
-                                    shift >= 32 ? 0xffffffffu : ((1u << shift) - 1u));
-      if (nbin == need) {  // the whole bin is taken
-        Kb = bin_lo - 1u;  // bin_lo > kmin >= 1 unless the bin is the lowest
-        cb = INT_MAX;
-        if (bin_lo == 0u) Kb = 0u;
-        break;
-      }
-      if (shift == 0 || bin_span == 0u) {
-        // one key value: the `need` lowest ids holding it
-        Kb = bin_lo;
-        int eq_base = 0;
-        for (int ch = 0; ch < nch; ++ch) {
-          uint32_t kk[16];
-          if (ch == 0) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) kk[j] = k0[j];
-          } else {
-            load16(ch, kk);
-          }
-          int ne = 0;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) ne += (kk[j] == bin_lo);
-          int2 t2;
-          const int before = eq_base + cscan2(make_int2(ne, 0), S, &t2, buf).x;
-          eq_base += t2.x;
-          if (before < need && need <= before + ne) {
-            int x = before;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (kk[j] == bin_lo && ++x == need) S.u.sel.res[3] = ch * kSelChunk + tid * 16 + j;
-            }
-          }
+    };
+    boundary(r_eff);
+    const int bstar = S.u.sel.res[0];
+    int need = r_eff - S.u.sel.res[1];
+    const int nbin = S.u.sel.res[2];
+    // rank the keys of a narrow range exactly: composite (key << 32 | ~id),
+    // larger first; the need-th is the threshold
+    auto rank_exact = [&](auto&& in_range) {
+      visit([&](uint32_t k, int id) {
+        if (k != 0u && in_range(k)) {
+          const int p = atomicAdd(&S.u.sel.ncand, 1);
+          if (p < kCand)
+            S.u.sel.cand[p] =
+                ((unsigned long long)k << 32) | (unsigned long long)(0xffffffffu - (uint32_t)id);
         }
-        csync();
-        cb = S.u.sel.res[3];
-        break;
+      });
+      csync();
+      const int nc = min(S.u.sel.ncand, kCand);
+      if (tid < nc) {
+        const unsigned long long mine = S.u.sel.cand[tid];
+        int rank = 0;
+        for (int j = 0; j < nc; ++j) rank += (int)(S.u.sel.cand[j] > mine);
+        if (rank == need - 1) {
+          S.u.sel.res[0] = (int)(uint32_t)(mine >> 32);
+          S.u.sel.res[1] = (int)(0xffffffffu - (uint32_t)mine);
+        }
       }
-      if (nbin <= kCand) {
-        // rank the bin's keys exactly: composite (key << 32 | ~id), larger first
+      csync();
+      Kb = (uint32_t)S.u.sel.res[0];
+      cb = S.u.sel.res[1];
+    };
+    if (nbin <= kCand) {
+      rank_exact([&](uint32_t k) { return bin_of(k) == bstar; });
+    } else {
+      // 3'. a crowded bin (ties or a pathological spread): its key range, then
+      // histograms of that range, kBins equal bins at a time
+      int nb2 = 0;
+      uint32_t lo = 0xffffffffu, hi = 0u;
+      visit([&](uint32_t k, int) {
+        if (k != 0u && bin_of(k) == bstar) {
+          lo = min(lo, k);
+          hi = max(hi, k);
+        }
+      });
+      block_count_range(nb2, hi, lo);
+      uint32_t span = hi - lo;
+      for (int iter = 0; iter < 8; ++iter) {
+        int shift = 0;
+        while ((span >> shift) >= (uint32_t)kBins) ++shift;
+        for (int i = tid; i < kBins; i += kCT) S.u.sel.hist[i] = 0;
+        if (tid == 0) S.u.sel.ncand = 0;
+        csync();
         {
-          const uint32_t l0 = bin_lo, sp = bin_span;
-          visit([&](uint32_t k, int id) {
-            if (k != 0u && k - l0 <= sp) {
-              const int p = atomicAdd(&S.u.sel.ncand, 1);
-              if (p < kCand)
-                S.u.sel.cand[p] =
-                    ((unsigned long long)k << 32) | (unsigned long long)(0xffffffffu - (uint32_t)id);
-            }
+          const uint32_t l0 = lo, sp = span;
+          const int sh = shift;
+          visit([&](uint32_t k, int) {
+            if (k != 0u && k - l0 <= sp) atomicAdd(&S.u.sel.hist[(k - l0) >> sh], 1);
           });
         }
         csync();
-        const int nc = min(S.u.sel.ncand, kCand);
-        if (tid < nc) {
-          const unsigned long long mine = S.u.sel.cand[tid];
-          int rank = 0;
-          for (int j = 0; j < nc; ++j) rank += (int)(S.u.sel.cand[j] > mine);
-          if (rank == need - 1) {
-            S.u.sel.res[0] = (int)(uint32_t)(mine >> 32);
-            S.u.sel.res[1] = (int)(0xffffffffu - (uint32_t)mine);
-          }
+        boundary(need);
+        const int bs = S.u.sel.res[0], above = S.u.sel.res[1], nbn = S.u.sel.res[2];
+        need -= above;
+        const uint32_t bin_lo = lo + ((uint32_t)bs << shift);
+        const uint32_t bin_span = min(span - ((uint32_t)bs << shift), (1u << shift) - 1u);
+        if (nbn <= kCand) {
+          const uint32_t l0 = bin_lo, sp = bin_span;
+          rank_exact([&](uint32_t k) { return k - l0 <= sp; });
+          break;
         }
-        csync();
-        Kb = (uint32_t)S.u.sel.res[0];
-        cb = S.u.sel.res[1];
-        break;
+        if (shift == 0 || bin_span == 0u) {
+          // one key value: the `need` lowest ids holding it
+          Kb = bin_lo;
+          int eq_base = 0;
+          for (int ch = 0; ch < nch; ++ch) {
+            int ne = 0;
+            auto cnt_eq = [&](uint32_t k, int) { ne += (k == bin_lo); };
+            if (ch == 0) {
+#pragma unroll 4
+              for (int j = 0; j < 16; ++j) cnt_eq(S.u.sel.key[j][tid], 0);
+            } else {
+              chunk_keys(ch, cnt_eq);
+            }
+            int2 t2;
+            const int before = eq_base + cscan2(make_int2(ne, 0), S, &t2, buf).x;
+            eq_base += t2.x;
+            if (before < need && need <= before + ne) {
+              int x = before;
+              auto find = [&](uint32_t k, int id) {
+                if (k == bin_lo && ++x == need) S.u.sel.res[3] = id;
+              };
+              if (ch == 0) {
+                for (int j = 0; j < 16; ++j) find(S.u.sel.key[j][tid], tid * 16 + j);
+              } else {
+                chunk_keys(ch, find);
+              }
+            }
+          }
+          csync();
+          cb = S.u.sel.res[3];
+          break;
+        }
+        lo = bin_lo;  // narrow to the boundary bin
+        span = bin_span;
       }
-      lo = bin_lo;  // narrow to the boundary bin
-      span = bin_span;
     }
   }
 
-  // ordered compaction (ids ascending) with the token offsets
+  // 4. ids in ascending order, then each selected cluster's size, row, score
   const int rsel0 = bh * rs;
   int* ids = a.sel_ids + rsel0;
   int* rows = a.sel_rows + rsel0;
@@ -587,60 +630,66 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   int* pre = a.sel_pre + rsel0;
   float* ssel = a.sel_sc + rsel0;
   int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
-  int sel_base = 0, tok_base = 0;
+  int sel_base = 0;
   if (r_eff > 0) {
     for (int ch = 0; ch < nch; ++ch) {
-      uint32_t kk[16];
-      if (ch == 0) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) kk[j] = k0[j];
-      } else {
-        load16(ch, kk);
-      }
-      const int c0 = ch * kSelChunk + tid * 16;
-      uint32_t selmask = 0u;
-      int nsel = 0, ntok = 0;
-      int nj[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t k = kk[j];
-        nj[j] = 0;
-        if (k != 0u && (k > Kb || (k == Kb && c0 + j <= cb))) {
-          selmask |= 1u << j;
+      uint32_t mask = 0u;
+      int nsel = 0;
+      auto mark = [&](uint32_t k, int id) {
+        if (k != 0u && (k > Kb || (k == Kb && id <= cb))) {
+          mask |= 1u << (id & 15);
           ++nsel;
-          nj[j] = __ldg(sz + c0 + j);
-          if (nj[j] < 0) nj[j] = 0;
-          ntok += nj[j];
         }
+      };
+      if (ch == 0) {
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) mark(S.u.sel.key[j][tid], tid * 16 + j);
+      } else {
+        chunk_keys(ch, mark);
       }
       int2 tot;
-      const int2 ex = cscan2(make_int2(nsel, ntok), S, &tot, buf);
-      int pos = sel_base + ex.x, tk = tok_base + ex.y;
+      int pos = sel_base + cscan2(make_int2(nsel, 0), S, &tot, buf).x;
       sel_base += tot.x;
-      tok_base += tot.y;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if ((selmask & (1u << j)) && pos < r) {
-          const int c = c0 + j;
-          int n = nj[j], row = __ldg(off + c);
-          if (row < 0 || (long long)row + n > a.N_idx) {
-            report(a.status, WI_ERR_INDEX_MISMATCH);  // inconsistent index: stage nothing
-            n = 0;
-            row = 0;
-          }
-          ids[pos] = c;
-          rows[pos] = row;
-          cnts[pos] = n;
-          pre[pos] = tk;
-          ssel[pos] = key_float(kk[j]);
-          if (topk) topk[pos] = c;
-          ++pos;
-          tk += nj[j];
+      const int c0 = ch * kSelChunk + tid * 16;
+      while (mask) {
+        const int j = __ffs(mask) - 1;
+        mask &= mask - 1;
+        if (pos < r) {
+          ids[pos] = c0 + j;
+          if (topk) topk[pos] = c0 + j;
         }
+        ++pos;
       }
     }
   }
   const int nsel_tot = min(sel_base, r);  // == r_eff
+  csync();  // the ids are written (and visible to the block)
+  int tok_base = 0;
+  for (int i0 = 0; i0 < nsel_tot; i0 += kCT) {
+    const int i = i0 + tid;
+    int n = 0, row = 0;
+    float sv = -INFINITY;
+    if (i < nsel_tot) {
+      const int c = ids[i];
+      n = __ldg(sz + c);
+      row = __ldg(off + c);
+      sv = __ldcg(sc + c);
+      if (n < 0 || row < 0 || (long long)row + n > a.N_idx) {
+        report(a.status, WI_ERR_INDEX_MISMATCH);  // inconsistent index: stage nothing
+        n = 0;
+        row = 0;
+      }
+    }
+    int2 tot;
+    const int ex = cscan2(make_int2(n, 0), S, &tot, buf).x;
+    if (i < nsel_tot) {
+      rows[i] = row;
+      cnts[i] = n;
+      pre[i] = tok_base + ex;
+      ssel[i] = sv;
+    }
+    tok_base += tot.x;
+  }
   for (int i = nsel_tot + tid; i < rs; i += kCT) {
     ids[i] = -1;
     rows[i] = 0;
@@ -741,32 +790,36 @@ __device__ void merge_head(const DecodeArgs& a, DecSmem& S, int bh, int n_est, i
 // boundaries.  Computed by the producer warp into S.bnd.
 __device__ void partition(const DecodeArgs& a, DecSmem& S, long long Ttot) {
   const int lane = threadIdx.x & 31;
-  const double avg = ((double)a.static_units * kTokPerUnit + (double)Ttot) / a.nb;
-  double carry = 0.0;
-  double wsum = 0.0;
-  // total weight
+  // in tokens, scaled by nb: w_b * nb = max(0, total - nb * static_b)
+  const long long total = a.static_units * kTokPerUnit + Ttot;
+  long long wsum = 0;
   for (int b0 = 0; b0 < a.nb; b0 += 32) {
     const int b = b0 + lane;
-    const double w = b < a.nb ? fmax(0.0, avg - (double)a.static_w[b] * kTokPerUnit) : 0.0;
-    double x = w;
+    long long w = b < a.nb ? total - (long long)a.nb * S.static_w[b] * kTokPerUnit : 0;
+    w = w > 0 ? w : 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-    wsum += x;
+    for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(kFull, w, o);
+    wsum += w;
   }
+  // shares proportional to w (float ratios: the same operations in every
+  // block give the same, monotone boundaries)
+  const float scale = wsum > 0 ? (float)Ttot / (float)wsum : 0.f;
+  long long carry = 0;
   for (int b0 = 0; b0 < a.nb; b0 += 32) {
     const int b = b0 + lane;
-    const double w = b < a.nb ? fmax(0.0, avg - (double)a.static_w[b] * kTokPerUnit) : 0.0;
-    double incl = w;
+    long long w = b < a.nb ? total - (long long)a.nb * S.static_w[b] * kTokPerUnit : 0;
+    w = w > 0 ? w : 0;
+    long long incl = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double t = __shfl_up_sync(kFull, incl, o);
+      const long long t = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += t;
     }
-    const double excl = carry + incl - w;
+    const long long excl = carry + incl - w;
     if (b < a.nb) {
-      long long t = wsum > 0.0 ? (long long)(excl / wsum * (double)Ttot) : 0;
+      long long t = (long long)((float)excl * scale);
       t = (t / kTile) * kTile;
-      S.bnd[b] = (int)min(t, Ttot);
+      S.bnd[b] = (int)(t < Ttot ? t : Ttot);
     }
     carry += __shfl_sync(kFull, incl, 31);
   }
@@ -817,79 +870,113 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
     else bulk_g2s(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]));
   };
 
-  const bool side_bulk = (a.C & 3) == 0;  // rows of sizes start 16-byte aligned
-  // 1. index chunks: centroid-key tiles, then value-sum tiles
-  if (a.stages & kStageScore) {
-    for (int rd = 0; rd < a.rounds; ++rd) {
-      const int j = rd * a.nb + (int)blockIdx.x;
-      if (j >= a.nchunks) break;
-      const int n = chunk_tiles(a, j);
-      for (int pass = 0; pass < 2; ++pass) {
-        const float* src = pass == 0 ? a.kbar : a.vsum;
-        for (int i = 0; i < n; ++i) {
-          const int T = j * a.Q + i;
-          const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
-          const int nrows = min(kTile, a.C - c0);
-          int stage;
-          if (!slot(stage)) return;
-          uint32_t bytes = (uint32_t)nrows * 512u;
-          const bool bulk_n = side_bulk && (nrows & 3) == 0;
-          if (pass == 0) {
-            bytes += (uint32_t)G * kD * 2;
-            if (bulk_n) {
-              bytes += (uint32_t)nrows * 4u;
-            } else {
-              for (int c = lane; c < kTile; c += 32)
-                S.side[stage].n[c] = c < nrows ? __ldg(a.size + (size_t)bg * a.C + c0 + c) : 0;
+  // 1-2. index and steady tiles: lane 0 alone, addresses advanced
+  // incrementally, one bulk copy per operand; the other lanes wait
+  if (lane == 0) {
+    bool inj = inject;
+    // next ring slot; false once this block aborted
+    auto wait_slot = [&](int& stage) -> bool {
+      stage = (int)(seq % kStages);
+      if (*(volatile int*)&S.abort) return false;
+      if (seq >= (uint32_t)kStages &&
+          !stage_wait(smem_addr(&S.empty[stage]), ((seq / kStages) - 1u) & 1u, a.status, &S.abort))
+        return false;
+      fence_proxy_async_smem();
+      return true;
+    };
+    auto issue = [&](void* dst, const void* src, uint32_t bytes, int stage) {
+      if (!inj) bulk_g2s(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]));
+    };
+    auto done_tile = [&]() {
+      inj = false;  // the test hook drops the copies of the first tile only
+      S.issued = (int)(++seq);
+    };
+    bool ok = true;
+    const bool side_bulk = (a.C & 3) == 0;  // rows of sizes start 16-byte aligned
+    if (a.stages & kStageScore) {
+      for (int rd = 0; rd < a.rounds && ok; ++rd) {
+        const int j = rd * a.nb + (int)blockIdx.x;
+        if (j >= a.nchunks) break;
+        const int n = chunk_tiles(a, j);
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+          const float* src = pass == 0 ? a.kbar : a.vsum;
+          int bg = (j * a.Q) / a.tpg, c0 = (j * a.Q - bg * a.tpg) * kTile;
+          int q_bg = -1;  // the group whose query rows were staged last
+          for (int i = 0; i < n; ++i) {
+            const int nrows = min(kTile, a.C - c0);
+            int stage;
+            if (!wait_slot(stage)) {
+              ok = false;
+              break;
+            }
+            const size_t row0 = (size_t)bg * a.C + c0;
+            uint32_t bytes = (uint32_t)nrows * 512u;
+            const bool bulk_n = side_bulk && (nrows & 3) == 0;
+            const bool with_q = pass == 0 && bg != q_bg;
+            if (pass == 0) {
+              if (with_q) bytes += (uint32_t)G * kD * 2;
+              if (bulk_n) {
+                bytes += (uint32_t)nrows * 4u;
+              } else {  // ragged rows of sizes: plain loads before the tile is posted
+                for (int c = 0; c < kTile; ++c) S.side[stage].n[c] = c < nrows ? __ldg(a.size + row0 + c) : 0;
+              }
+            }
+            mbar_arrive_expect_tx(smem_addr(&S.full[stage]), bytes);
+            issue(S.ring[stage], src + row0 * kD, (uint32_t)nrows * 512u, stage);
+            if (with_q) {  // the consumers read the query rows with a group's first tile
+              const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+              issue(S.qs[stage], a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD,
+                    (uint32_t)G * kD * 2, stage);
+              q_bg = bg;
+            }
+            if (pass == 0 && bulk_n)
+              issue(S.side[stage].n, a.size + row0, (uint32_t)nrows * 4u, stage);
+            done_tile();
+            c0 += kTile;
+            if (c0 >= a.C) {
+              c0 = 0;
+              ++bg;
             }
           }
-          post(stage, bytes);
-          if (lane == 0) copy_to(S.ring[stage], src + ((size_t)bg * a.C + c0) * kD,
-                                 (uint32_t)nrows * 512u, stage);
-          if (pass == 0) {
-            const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-            if (lane == 1)
-              copy_to(S.qs[stage], a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD,
-                      (uint32_t)G * kD * 2, stage);
-            if (lane == 2 && bulk_n)
-              copy_to(S.side[stage].n, a.size + (size_t)bg * a.C + c0, (uint32_t)nrows * 4u,
-                      stage);
-          }
-          commit();
         }
       }
     }
-  }
-  if (!(a.stages & kStageAttend)) return;
-
-  // 2. steady tiles: K/V rows of one KV group, with the group's query rows
-  const long long nst = (long long)a.B * a.Hkv * a.tph;
-  for (long long t = a.nb - 1 - (long long)blockIdx.x; t < nst; t += a.nb) {
-    int stage;
-    if (!slot(stage)) return;
-    const int bg = (int)(t / a.tph), i = (int)(t - (long long)bg * a.tph);
-    const int u0 = i * kTile, u1 = min(ns, u0 + kTile), n = u1 - u0;
-    const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-    post(stage, (uint32_t)n * 512u + (uint32_t)G * kD * 2u);
-    // steady index u < sink is position u; the rest are N - window + (u - sink)
-    const int a1 = min(u1, a.sink);
-    if (lane < 2 && u0 < a1) {
-      const uint16_t* base = (lane == 0 ? a.K : a.V) + ((size_t)bg * a.N + u0) * kD;
-      copy_to(S.ring[stage] + (lane == 0 ? 0u : kStageBytes / 2), base,
-              (uint32_t)(a1 - u0) * 256u, stage);
-    }
-    const int b0 = max(u0, a.sink);
-    if (lane >= 2 && lane < 4 && b0 < u1) {
-      const int row = a.N - a.window + (b0 - a.sink);
-      const uint16_t* base = (lane == 2 ? a.K : a.V) + ((size_t)bg * a.N + row) * kD;
-      copy_to(S.ring[stage] + (uint32_t)(b0 - u0) * 256u + (lane == 2 ? 0u : kStageBytes / 2),
-              base, (uint32_t)(u1 - b0) * 256u, stage);
-    }
-    if (lane == 4)
-      copy_to(S.qs[stage], a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD, (uint32_t)G * kD * 2,
+    // steady tiles: K/V rows of one KV group, with the group's query rows;
+    // steady index u < sink is position u, the rest are N - window + (u - sink)
+    if (ok && (a.stages & kStageAttend)) {
+      const int nst = a.B * a.Hkv * a.tph;
+      for (int t = a.nb - 1 - (int)blockIdx.x; t < nst; t += a.nb) {
+        int stage;
+        if (!wait_slot(stage)) break;
+        const int bg = t / a.tph, i = t - bg * a.tph;
+        const int u0 = i * kTile, u1 = min(ns, u0 + kTile), n = u1 - u0;
+        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+        mbar_arrive_expect_tx(smem_addr(&S.full[stage]), (uint32_t)n * 512u + (uint32_t)G * kD * 2u);
+        const int a1 = min(u1, a.sink);
+        if (u0 < a1) {
+          const size_t r0 = (size_t)bg * a.N + u0;
+          issue(S.ring[stage], a.K + r0 * kD, (uint32_t)(a1 - u0) * 256u, stage);
+          issue(S.ring[stage] + kStageBytes / 2, a.V + r0 * kD, (uint32_t)(a1 - u0) * 256u, stage);
+        }
+        const int b0 = max(u0, a.sink);
+        if (b0 < u1) {
+          const size_t r0 = (size_t)bg * a.N + (a.N - a.window + (b0 - a.sink));
+          const uint32_t d = (uint32_t)(b0 - u0) * 256u;
+          issue(S.ring[stage] + d, a.K + r0 * kD, (uint32_t)(u1 - b0) * 256u, stage);
+          issue(S.ring[stage] + kStageBytes / 2 + d, a.V + r0 * kD, (uint32_t)(u1 - b0) * 256u,
+                stage);
+        }
+        issue(S.qs[stage], a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD, (uint32_t)G * kD * 2,
               stage);
-    commit();
+        done_tile();
+      }
+    }
+    inject = inj;
   }
+  __syncwarp();
+  seq = __shfl_sync(kFull, seq, 0);
+  inject = __shfl_sync(kFull, (int)inject, 0) != 0;
+  if (*(volatile int*)&S.abort || !(a.stages & kStageAttend)) return;
 
   // 3. retrieval tiles of the block's share of the retrieved tokens
   if (a.r > 0) {
@@ -1194,55 +1281,64 @@ __device__ bool wait_count_all(const DecodeArgs& a, DecSmem& S, const unsigned* 
 // into the workspace and the block's chunk copy; then the groups' scored-tile
 // counts are published.
 template <int G>
-__device__ __noinline__ void kbar_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n) {
+__device__ __forceinline__ void kbar_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L4 = 4 * G;
   const int jr = lane_row<G>(lane), hr = lane_head<G>(lane);
-  // a. centroid-key tiles: scores of the group's G heads
+  const int C = a.C;
+  // tile i of the chunk: KV group bg, first cluster c0 (advanced per tile)
+  int bg = (j * a.Q) / a.tpg, c0 = (j * a.Q - bg * a.tpg) * kTile;
+  int cur_bg = -1;
+  float4 qs[G];           // this lane's 4 dimensions of the group's query rows, scaled
+  float* srow = nullptr;  // scores row of this lane's head
+#pragma unroll
+  for (int h = 0; h < G; ++h) qs[h] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = 0; i < n; ++i) {
-    const int T = j * a.Q + i;
-    const int bg = T / a.tpg, c0 = (T - bg * a.tpg) * kTile;
-    const int nrows = min(kTile, a.C - c0);
+    const int nrows = min(kTile, C - c0);
     int stage;
-    float4 k[4];
-    uint2 q[G];
-    int nsz = 0;
-    const bool got = acquire(a, S, rg, stage);
-    if (got) {
+    if (acquire(a, S, rg, stage)) {
+      float4 k[4];
       const float* kb = reinterpret_cast<const float*>(S.ring[stage]);
 #pragma unroll
       for (int r4 = 0; r4 < 4; ++r4) {
         const int row = warp * 4 + r4;
         k[r4] = row < nrows ? lds4(kb + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      if (bg != cur_bg) {  // the group's query rows come with its first tile
 #pragma unroll
-      for (int h = 0; h < G; ++h) q[h] = lds2(S.qs[stage] + h * kD * 2 + lane * 8);
-      nsz = S.side[stage].n[warp * 4 + jr];
+        for (int h = 0; h < G; ++h) {
+          const float4 qf = bf4(lds2(S.qs[stage] + h * kD * 2 + lane * 8));
+          qs[h] = make_float4(qf.x * a.scale, qf.y * a.scale, qf.z * a.scale, qf.w * a.scale);
+        }
+        cur_bg = bg;
+        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+        srow = a.scores + ((size_t)b * a.Hq + (size_t)g * G + hr) * C;
+      }
+      const int nsz = S.side[stage].n[warp * 4 + jr];
       release(S, rg, stage);
       float v[4 * G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float4 qf = bf4(q[h]);
-        const float q0 = qf.x * a.scale, q1 = qf.y * a.scale, q2 = qf.z * a.scale,
-                    q3 = qf.w * a.scale;
 #pragma unroll
         for (int r4 = 0; r4 < 4; ++r4)
-          v[r4 * G + h] = k[r4].x * q0 + k[r4].y * q1 + k[r4].z * q2 + k[r4].w * q3;
+          v[r4 * G + h] = k[r4].x * qs[h].x + k[r4].y * qs[h].y + k[r4].z * qs[h].z + k[r4].w * qs[h].w;
       }
       const float tot = reduce_scatter<4 * G>(v, lane);
       const int row = warp * 4 + jr;
       const float s = (row < nrows && nsz > 0) ? tot : -INFINITY;
       if (lane < L4) {
-        if (row < nrows) {
-          const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-          a.scores[((size_t)b * a.Hq + (size_t)g * G + hr) * a.C + c0 + row] = s;
-        }
+        if (row < nrows) srow[c0 + row] = s;
         S.a.chunk.sc[i][warp][lane] = s;
         if (hr == 0) S.a.chunk.n[i][warp][jr] = row < nrows ? nsz : 0;
       }
     } else if (lane < L4) {
       S.a.chunk.sc[i][warp][lane] = -INFINITY;
       if (hr == 0) S.a.chunk.n[i][warp][jr] = 0;
+    }
+    c0 += kTile;
+    if (c0 >= C) {
+      c0 = 0;
+      ++bg;
     }
   }
   if (n > 0) {
@@ -1262,7 +1358,7 @@ __device__ __noinline__ void kbar_tiles(const DecodeArgs& a, DecSmem& S, Ring& r
 // The selections assigned to this block in round rd (heads in order): each
 // once its KV group is fully scored.
 template <int G>
-__device__ __noinline__ void selections(const DecodeArgs& a, DecSmem& S, const Ring& rg, int rd) {
+__device__ __forceinline__ void selections(const DecodeArgs& a, DecSmem& S, const Ring& rg, int rd) {
   const int tid = threadIdx.x;
   const int blk = (int)blockIdx.x;
   // b. selections assigned to this block and round (heads in order)
@@ -1305,7 +1401,7 @@ __device__ __noinline__ void selections(const DecodeArgs& a, DecSmem& S, const R
 // against the warp's own maximum score of each KV group (a fixed reference:
 // no rescaling), one partial per (chunk, KV group, query head).
 template <int G>
-__device__ __noinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n) {
+__device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L4 = 4 * G;
   const int jr = lane_row<G>(lane), hr = lane_head<G>(lane);
@@ -1384,7 +1480,7 @@ __device__ __noinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring& r
 // Steady tiles of this block: the sink and local-window K/V rows of one KV
 // group, its G heads at once; one partial per (tile, head).
 template <int G>
-__device__ __noinline__ void steady_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg) {
+__device__ __forceinline__ void steady_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int blk = (int)blockIdx.x;
   const int jr = lane_row<G>(lane);
@@ -1440,7 +1536,7 @@ __device__ __noinline__ void steady_tiles(const DecodeArgs& a, DecSmem& S, Ring&
 // marker.  Every warp keeps its own softmax state; at the end of a head's
 // range the last warp to finish combines the 16 states into the piece's
 // partial (slot block + head) and publishes it.
-__device__ __noinline__ void retrieval_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg) {
+__device__ __forceinline__ void retrieval_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int blk = (int)blockIdx.x;
   // ---- 3. retrieval tiles: one head per tile; every warp keeps its own state
@@ -1566,17 +1662,17 @@ __device__ __noinline__ void retrieval_tiles(const DecodeArgs& a, DecSmem& S, Ri
 
 // Merges of heads blk, blk + nb, ...: once every partial of the head is
 // published, the log-sum-exp combine into out and lse.
-__device__ __noinline__ void merges(const DecodeArgs& a, DecSmem& S) {
+__device__ __forceinline__ void merges(const DecodeArgs& a, DecSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int blk = (int)blockIdx.x;
-  const long long H = (long long)a.B * a.Hq;
-  for (long long bh = blk; bh < H; bh += a.nb) {
-    const int bg = (int)(bh / a.G);
+  const int H = a.B * a.Hq;
+  for (int bh = blk; bh < H; bh += a.nb) {
+    const int bg = bh / a.G;
     // this head's retrieval pieces: blocks whose share meets its tokens
     int P_lo = 0;
     {
       int part = 0;
-      for (long long h2 = tid; h2 < bh; h2 += kCT) part += __ldcg(a.head_tok + h2);
+      for (int h2 = tid; h2 < bh; h2 += kCT) part += __ldcg(a.head_tok + h2);
       part = __reduce_add_sync(kFull, part);
       if (lane == 0) S.u.merge.cnt[warp] = part;
       csync();
@@ -1600,7 +1696,7 @@ __device__ __noinline__ void merges(const DecodeArgs& a, DecSmem& S) {
     // estimate pieces are counted only when this launch wrote them
     const unsigned target = (unsigned)((a.fused ? n_est : 0) + a.tph + n_ret);
     if (!wait_count_all(a, S, a.head_cnt + bh, target)) break;
-    merge_head(a, S, (int)bh, n_est, e_lo, n_ret);
+    merge_head(a, S, bh, n_est, e_lo, n_ret);
     csync();  // S.u.merge.cnt is rewritten by the next head
   }
 }
@@ -1707,6 +1803,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   }
   if (tid < kPubSlots) S.pub[tid].ready = 0;
   if (tid < kSlots) S.slot_cnt[tid] = 0u;
+  for (int b = tid; b < a.nb; b += kThreads) S.static_w[b] = a.static_w[b];
   __syncthreads();
   if (tid >= kCT + 32) signaler(a, S);
   else if (tid >= kCT) producer<G>(a, S);

@@ -109,11 +109,12 @@ __host__ __device__ inline int chunk_tiles(const DecodeArgs& a, int j) {
   const int lo = j * a.Q, hi = lo + a.Q < a.nt ? lo + a.Q : a.nt;
   return hi > lo ? hi - lo : 0;
 }
+// (nt = B * Hkv * tpg < 2^31 is checked on the host: 32-bit arithmetic)
 __host__ __device__ inline int first_chunk(const DecodeArgs& a, int bg) {
-  return (int)((long long)bg * a.tpg / a.Q);
+  return bg * a.tpg / a.Q;
 }
 __host__ __device__ inline int last_chunk(const DecodeArgs& a, int bg) {
-  return (int)(((long long)bg * a.tpg + a.tpg - 1) / a.Q);
+  return (bg * a.tpg + a.tpg - 1) / a.Q;
 }
 // Head bh (b*Hq + h) of KV group bg = bh / G is selected by block
 // (last_chunk(bg) - bh % G) mod nb, after that block's centroid-key tiles of
@@ -127,8 +128,8 @@ __host__ __device__ inline int sel_round(const DecodeArgs& a, int bh) {
   return last_chunk(a, bh / a.G) / a.nb;
 }
 // Steady tile t (of B*Hkv*tph) is taken by block nb - 1 - t % nb.
-__host__ __device__ inline int steady_block(const DecodeArgs& a, long long t) {
-  return a.nb - 1 - (int)(t % a.nb);
+__host__ __device__ inline int steady_block(const DecodeArgs& a, int t) {
+  return a.nb - 1 - t % a.nb;
 }
 // Head bh is merged by block bh % nb.
 __host__ __device__ inline int merge_block(const DecodeArgs& a, int bh) { return bh % a.nb; }
