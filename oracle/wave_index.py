@@ -61,6 +61,8 @@ __all__ = [
     "build_index",
     "cluster_scores",
     "select_clusters",
+    "ranking_keys",
+    "reuse_groups",
     "decode_head",
     "decode",
 ]
@@ -285,25 +287,64 @@ def cluster_scores(q: np.ndarray, centroid_key: np.ndarray, size: np.ndarray,
     return np.where(size > 0, s, -np.inf)
 
 
+def ranking_keys(s: np.ndarray, size: np.ndarray, rank: str = "score") -> np.ndarray:
+    """The key clusters are ranked by for the retrieval zone.
+
+    * ``"score"``: s_c, the cluster's logit (RetroInfer summary §2.A.2: the
+      clusters most similar to the query);
+    * ``"mass"``: the estimated attention mass n_c e^{s_c} of the cluster,
+      compared in log space as s_c + ln n_c.  Reading: the "attention-aware"
+      index of the technical summary (ar) §2.a ranks by the share of the
+      softmax a cluster would take, which is what its estimate weighs; an
+      empty cluster has no mass (-inf)."""
+    if rank == "score":
+        return s
+    if rank != "mass":
+        raise ValueError(rank)
+    n = np.asarray(size, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        return np.where((n > 0) & np.isfinite(s), s + np.log(np.where(n > 0, n, 1.0)), -np.inf)
+
+
 def select_clusters(s: np.ndarray, r: int) -> np.ndarray:
-    """Retrieval zone: the r highest-scoring non-empty clusters, ordered by
-    (score descending, cluster id ascending); fewer when fewer are non-empty.
-    Returned sorted by id."""
+    """Retrieval zone: the r clusters with the largest key s (a score or a
+    ranking key), ordered by (key descending, cluster id ascending); clusters
+    whose key is -inf (empty) are never taken, so fewer when fewer are
+    non-empty.  Returned sorted by id."""
     ids = np.arange(s.shape[0])
     finite = np.isfinite(s)
     order = np.lexsort((ids[finite], -s[finite]))
     return np.sort(ids[finite][order][:r])
 
 
+def reuse_groups(q: np.ndarray, q_prev: np.ndarray, group: int, tau: float) -> np.ndarray:
+    """Speculative reuse with fine-grained correction (FreeKV technical
+    summary §2.A.1-2): the retrieval set of the previous decoding step is
+    reused while the query has not moved, and re-selected for the KV heads
+    whose queries did.  Reading: the similarity of a KV head is the smallest
+    cosine cos(q_t, q_{t-1}) over its query heads; it reuses iff that is at
+    least tau.
+
+    q, q_prev: [Hq, d] (one sequence).  Returns a bool per KV head."""
+    qn = np.linalg.norm(q, axis=1)
+    pn = np.linalg.norm(q_prev, axis=1)
+    dot = np.sum(q * q_prev, axis=1)
+    cos = np.divide(dot, qn * pn, out=np.zeros_like(dot), where=(qn > 0) & (pn > 0))
+    return cos.reshape(-1, group).min(axis=1) >= tau
+
+
 def decode_head(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np.ndarray],
                 sink: int, window: int, r: int, scale: float,
-                selected: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+                selected: Optional[np.ndarray] = None,
+                rank: str = "score") -> Dict[str, np.ndarray]:
     """Tripartite attention of one query q [d] over one KV head (K, V [N, d]).
 
     Steps (RetroInfer summary §2.A; technical summary (ar) §2.a):
 
     1. scores s_c of every cluster against the query;
-    2. retrieval zone T = the top-r clusters (or ``selected`` if given);
+    2. retrieval zone T = the top-r clusters by the ranking key (the score,
+       or the attention mass with ``rank="mass"``), or ``selected`` if given
+       (empty clusters in it attend nothing);
     3. exact token set S = steady zone + members of T, logits l_i = scale q.k_i;
     4. estimation zone E = non-empty clusters outside T: each member's logit is
        taken as its cluster's score, so cluster c contributes n_c e^{s_c} to
@@ -318,7 +359,10 @@ def decode_head(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np
     N = K.shape[0]
     size = index["size"]
     s = cluster_scores(q, index["centroid_key"], size, scale)
-    T = select_clusters(s, r) if selected is None else np.sort(np.asarray(selected, np.int64))
+    if selected is None:
+        T = select_clusters(ranking_keys(s, size, rank), r)
+    else:
+        T = np.unique(np.asarray(selected, np.int64))
     members = [index["perm"][index["offset"][c]:index["offset"][c + 1]] for c in T]
     S = np.concatenate([steady_positions(N, sink, window)] + members).astype(np.int64)
     logits = scale * (K[S] @ q)
@@ -349,11 +393,19 @@ def decode_head(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np
 
 def decode(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np.ndarray],
            sink: int, window: int, r: int, scale: Optional[float] = None,
-           heads: Optional[List[tuple]] = None) -> Dict[str, np.ndarray]:
+           heads: Optional[List[tuple]] = None, rank: str = "score",
+           prev_q: Optional[np.ndarray] = None, prev_selected: Optional[dict] = None,
+           tau: float = 1.0) -> Dict[str, np.ndarray]:
     """Decode attention for q [B, Hq, d] against K, V [B, Hkv, N, d] and a
     per-(b, kv head) index with leading [B, Hkv] axes.  Query head h reads KV
     head h // (Hq / Hkv) (grouped-query attention).  ``heads`` restricts the
-    work to a list of (b, h) pairs; the other rows of the result stay NaN."""
+    work to a list of (b, h) pairs; the other rows of the result stay NaN.
+
+    ``rank`` picks the ranking key of the retrieval zone (``ranking_keys``).
+    With ``prev_q`` [B, Hq, d] and ``prev_selected`` ({(b, h): ids}) the
+    previous step's selection is reused by every KV head that
+    ``reuse_groups`` keeps at threshold ``tau``; the others select afresh.
+    ``reused`` [B, Hkv] reports the decision."""
     B, Hq, d = q.shape
     Hkv = K.shape[1]
     group = Hq // Hkv
@@ -361,13 +413,19 @@ def decode(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np.ndar
     out = np.full((B, Hq, d), np.nan)
     lse = np.full((B, Hq), np.nan)
     sel = {}
+    reused = np.zeros((B, Hkv), dtype=bool)
+    if prev_q is not None:
+        for b in range(B):
+            reused[b] = reuse_groups(q[b], prev_q[b], group, tau)
     todo = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]
     for b, h in todo:
         g = h // group
         ih = {key: index[key][b, g] for key in ("size", "centroid_key", "value_sum", "perm",
                                                  "offset")}
-        res = decode_head(q[b, h], K[b, g], V[b, g], ih, sink, window, r, scale)
+        given = prev_selected[(b, h)] if reused[b, g] else None
+        res = decode_head(q[b, h], K[b, g], V[b, g], ih, sink, window, r, scale,
+                          selected=given, rank=rank)
         out[b, h] = res["out"]
         lse[b, h] = res["lse"]
         sel[(b, h)] = res["selected"]
-    return {"out": out, "lse": lse, "selected": sel}
+    return {"out": out, "lse": lse, "selected": sel, "reused": reused}

@@ -405,3 +405,122 @@ def test_decode_wrapper_budgeted_rows_and_head_subset():
     np.testing.assert_array_equal(part["out"][0, 5], full["out"][0, 5])
     assert np.isnan(part["out"][0, 0]).all() and np.isnan(part["lse"][1, 1])
     assert set(part["selected"]) == {(1, 6), (0, 5)}
+
+
+# ---------------------------------------------------------------- ranking and reuse
+
+def test_mass_ranking_bruteforce_products():
+    # The mass key must order clusters like the product n_c e^{s_c} itself
+    # (computed here without logarithms, ranking by a Python sort of
+    # (-mass, id)); a dropped ln n_c or a sign slip orders them differently.
+    rng = np.random.default_rng(40)
+    for trial in range(50):
+        C = int(rng.integers(1, 30))
+        s = rng.standard_normal(C) * 2.0
+        n = rng.integers(0, 9, C)
+        s[n == 0] = -np.inf
+        r = int(rng.integers(0, C + 2))
+        mass = [(float(n[c]) * math.exp(s[c])) if n[c] > 0 else None for c in range(C)]
+        ranked = sorted((c for c in range(C) if mass[c] is not None), key=lambda c: (-mass[c], c))
+        got = wi.select_clusters(wi.ranking_keys(s, n, "mass"), r)
+        assert got.tolist() == sorted(ranked[:r]), trial
+
+
+def test_mass_ranking_hand_case_and_equal_sizes():
+    # A big cluster scoring a little below a small one carries more mass:
+    # 40 e^{1.0} > 2 e^{2.0}.  Score ranking takes the small one, mass
+    # ranking the big one.
+    s = np.array([2.0, 1.0, -np.inf, 0.0])
+    n = np.array([2, 40, 0, 1])
+    assert wi.select_clusters(wi.ranking_keys(s, n, "score"), 1).tolist() == [0]
+    assert wi.select_clusters(wi.ranking_keys(s, n, "mass"), 1).tolist() == [1]
+    assert wi.select_clusters(wi.ranking_keys(s, n, "mass"), 9).tolist() == [0, 1, 3]
+    # with every cluster the same size the two rankings take the same set
+    rng = np.random.default_rng(41)
+    s = rng.standard_normal(64)
+    for r in (1, 7, 64):
+        assert np.array_equal(wi.select_clusters(wi.ranking_keys(s, np.full(64, 5), "mass"), r),
+                              wi.select_clusters(s, r))
+    with pytest.raises(ValueError):
+        wi.ranking_keys(s, np.full(64, 5), "other")
+
+
+def test_mass_ranking_decode_full_budget_and_given_set():
+    # Whatever the ranking, a full budget is exact attention; below it the
+    # result is the tripartite attention over the set the mass key selects.
+    K, V, q, idx = small_case(seed=42, d=64)
+    C = idx["size"].shape[0]
+    full = wi.decode_head(q, K, V, idx, 4, 32, C, 0.15, rank="mass")
+    ref, lse = sdpa64(q, K, V, 0.15)
+    np.testing.assert_allclose(full["out"], ref, rtol=1e-11, atol=1e-13)
+    assert abs(full["lse"] - lse) < 1e-11
+    part = wi.decode_head(q, K, V, idx, 4, 32, 5, 0.15, rank="mass")
+    s = part["scores"]
+    assert part["selected"].tolist() == wi.select_clusters(wi.ranking_keys(s, idx["size"], "mass"), 5).tolist()
+    same = wi.decode_head(q, K, V, idx, 4, 32, 5, 0.15, selected=part["selected"])
+    np.testing.assert_array_equal(same["out"], part["out"])
+
+
+def test_reuse_cosine_closed_form():
+    # cos((1,0),(1,1)) = 1/sqrt(2) = 0.7071...; a group's similarity is its
+    # least similar query head; a zero query has no direction (cosine 0).
+    q = np.array([[1.0, 0.0], [3.0, 0.0], [1.0, 0.0], [0.0, 0.0]])
+    p = np.array([[1.0, 1.0], [6.0, 0.0], [2.0, 0.0], [1.0, 0.0]])
+    assert wi.reuse_groups(q, p, 2, 0.707).tolist() == [True, False]
+    assert wi.reuse_groups(q, p, 2, 0.7072).tolist() == [False, False]
+    assert wi.reuse_groups(q, p, 2, 0.0).tolist() == [True, True]
+    assert wi.reuse_groups(q, p, 1, 0.9).tolist() == [False, True, True, False]
+    assert wi.reuse_groups(q, -p, 4, -1.5).tolist() == [True]
+
+
+def test_reuse_threshold_extremes():
+    # tau > 1: no cosine reaches it, so every head selects afresh and the
+    # result is the plain decode; tau <= -1 (here -2, clear of rounding):
+    # every head reuses, which is decode_head over the previous step's sets.
+    K, V, q, idx, z = _gqa_case(seed=43)
+    rng = np.random.default_rng(44)
+    q_prev = q + 0.3 * bf16_vals(rng, q.shape)
+    r = 4
+    prev = wi.decode(q_prev, K, V, idx, z["sink"], z["window"], r, 0.2)
+    plain = wi.decode(q, K, V, idx, z["sink"], z["window"], r, 0.2)
+    fresh = wi.decode(q, K, V, idx, z["sink"], z["window"], r, 0.2, prev_q=q_prev,
+                      prev_selected=prev["selected"], tau=1.5)
+    assert not fresh["reused"].any()
+    np.testing.assert_array_equal(fresh["out"], plain["out"])
+    kept = wi.decode(q, K, V, idx, z["sink"], z["window"], r, 0.2, prev_q=q_prev,
+                     prev_selected=prev["selected"], tau=-2.0)
+    assert kept["reused"].all()
+    B, Hq, _ = q.shape
+    group = Hq // K.shape[1]
+    differs = 0
+    for b in range(B):
+        for h in range(Hq):
+            g = h // group
+            hi = {key: idx[key][b, g] for key in ("size", "centroid_key", "value_sum", "perm",
+                                                  "offset")}
+            ref = wi.decode_head(q[b, h], K[b, g], V[b, g], hi, z["sink"], z["window"], r, 0.2,
+                                 selected=prev["selected"][(b, h)])
+            np.testing.assert_array_equal(kept["out"][b, h], ref["out"])
+            assert kept["selected"][(b, h)].tolist() == prev["selected"][(b, h)].tolist()
+            differs += set(prev["selected"][(b, h)].tolist()) != set(plain["selected"][(b, h)].tolist())
+    assert differs > 0  # the perturbation moved some selections, so reuse is visible
+
+
+def test_reuse_per_group_decision():
+    # Group 0's queries are unchanged (cosine 1), group 1 has one query head
+    # reversed (cosine -1): at tau = 0.5 only group 1 re-selects, and its
+    # heads equal the plain decode while group 0 keeps the given sets.
+    K, V, q, idx, z = _gqa_case(seed=45)
+    q_prev = q.copy()
+    q_prev[:, 5] = -q[:, 5]
+    B, Hq, _ = q.shape
+    r = 3
+    stale = {(b, h): np.array([0, 1, 2]) for b in range(B) for h in range(Hq)}
+    res = wi.decode(q, K, V, idx, z["sink"], z["window"], r, 0.2, prev_q=q_prev,
+                    prev_selected=stale, tau=0.5)
+    assert res["reused"].tolist() == [[True, False]] * B
+    plain = wi.decode(q, K, V, idx, z["sink"], z["window"], r, 0.2)
+    np.testing.assert_array_equal(res["out"][:, 4:], plain["out"][:, 4:])
+    for b in range(B):
+        for h in range(4):
+            assert res["selected"][(b, h)].tolist() == [0, 1, 2]
