@@ -192,13 +192,23 @@ def sync_status(workspace: torch.Tensor, stream=None) -> int:
 
 class Decoder:
     """Decode attention against one WaveIndex with fixed (Hq, r, scale); owns
-    its workspace and output buffers."""
+    its workspace and output buffers.
 
-    def __init__(self, index: WaveIndex, Hq: int, r: int, scale: Optional[float] = None):
+    rank: "score" (the r largest cluster scores) or "mass" (the r largest
+    estimated attention masses n_c e^{s_c}).  A call given prev_q and
+    prev_topk (the previous step's queries and returned ids; prev_topk may be
+    this decoder's own topk buffer) reuses the previous sets of every KV group
+    whose queries all keep a cosine >= tau with their previous query."""
+
+    def __init__(self, index: WaveIndex, Hq: int, r: int, scale: Optional[float] = None,
+                 rank: str = "score"):
         c = index.cfg
+        if rank not in L.RANKS:
+            raise ValueError("rank must be one of %s" % sorted(L.RANKS))
         self.index = index
         self.Hq = Hq
         self.r = r
+        self.rank = rank
         self.scale = 1.0 / math.sqrt(c.d) if scale is None else float(scale)
         self.params = L.DecodeParams(c.B, Hq, c.Hkv, c.N, c.d, c.sink, c.window, r, self.scale)
         lay = L.DecodeLayout()
@@ -210,6 +220,7 @@ class Decoder:
         self.out = torch.empty((c.B, Hq, c.d), dtype=torch.float32, device=dev)
         self.lse = torch.empty((c.B, Hq), dtype=torch.float32, device=dev)
         self.topk = torch.empty((c.B, Hq, max(r, 1)), dtype=torch.int32, device=dev)
+        self.reused = torch.zeros((c.B, Hq), dtype=torch.int32, device=dev)
 
     def _q(self, q):
         c = self.index.cfg
@@ -219,15 +230,33 @@ class Decoder:
         """The fused decode call on device buffers, captured as a CUDA graph."""
         return capture_graph(lambda: self(q, K, V, with_topk=with_topk), self.index.device)
 
-    def __call__(self, q, K, V, stream=None, with_topk: bool = True):
+    def __call__(self, q, K, V, stream=None, with_topk: bool = True, prev_q=None,
+                 prev_topk=None, tau: float = 1.0):
         """out [B,Hq,128] f32, lse [B,Hq] f32, topk ids [B,Hq,r] i32."""
         self._q(q)
         self.index._kv(K, V)
         topk = self.topk if (with_topk and self.r > 0) else None
-        L.check(L.lib().wi_decode_attention(
-            ctypes.byref(self.params), _ptr(q), _ptr(K), _ptr(V), ctypes.byref(self.index.struct),
-            _ptr(self.out), _ptr(self.lse), _ptr(topk), _ptr(self.workspace),
-            self.workspace.numel(), _stream(stream)), "wi_decode_attention")
+        if self.rank == "score" and prev_q is None:
+            L.check(L.lib().wi_decode_attention(
+                ctypes.byref(self.params), _ptr(q), _ptr(K), _ptr(V),
+                ctypes.byref(self.index.struct), _ptr(self.out), _ptr(self.lse), _ptr(topk),
+                _ptr(self.workspace), self.workspace.numel(), _stream(stream)),
+                "wi_decode_attention")
+        else:
+            c = self.index.cfg
+            opt = L.DecodeOptions(L.RANKS[self.rank], float(tau), None, None, _ptr(self.reused))
+            if prev_q is not None:
+                _need(prev_q, "prev_q", torch.bfloat16, (c.B, self.Hq, c.d), self.index.device)
+                if prev_topk is None:
+                    raise ValueError("prev_topk is required with prev_q")
+                _need(prev_topk, "prev_topk", torch.int32, (c.B, self.Hq, self.r),
+                      self.index.device)
+                opt.prev_q, opt.prev_topk = _ptr(prev_q), _ptr(prev_topk)
+            L.check(L.lib().wi_decode_attention_ex(
+                ctypes.byref(self.params), ctypes.byref(opt), _ptr(q), _ptr(K), _ptr(V),
+                ctypes.byref(self.index.struct), _ptr(self.out), _ptr(self.lse), _ptr(topk),
+                _ptr(self.workspace), self.workspace.numel(), _stream(stream)),
+                "wi_decode_attention_ex")
         return self.out, self.lse, (self.topk[..., :self.r] if topk is not None else None)
 
     # stages -------------------------------------------------------------

@@ -232,7 +232,7 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
 
 // Streamed-work equivalent of one per-head selection, in 4 KB units (the
 // scores and sizes it reads and the passes over them).
-unsigned selection_units(int C) { return 8u + (unsigned)(C / 128); }
+unsigned selection_units(int C) { return 24u + (unsigned)(C / 96); }
 
 }  // namespace
 
@@ -369,14 +369,37 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   return WI_OK;
 }
 
+// Host checks of the selection options (only the fused call takes them).
+int check_options(const wi_decode_options* o, const wi_decode_params* p) {
+  if (o == nullptr) return WI_OK;
+  if (o->rank != WI_RANK_SCORE && o->rank != WI_RANK_MASS) return WI_ERR_INVALID_ARG;
+  if (o->prev_q != nullptr && p != nullptr && p->r > 0) {
+    if (o->prev_topk == nullptr || !(o->tau == o->tau)) return WI_ERR_INVALID_ARG;
+    if (!aligned(o->prev_q, 16) || !aligned(o->prev_topk, 4)) return WI_ERR_ALIGNMENT;
+  }
+  if (!aligned(o->reused, 4)) return WI_ERR_ALIGNMENT;
+  return WI_OK;
+}
+
 int run_decode(const wi_decode_params* p, const void* q, const void* K, const void* V,
                const wi_index* index, float* out, float* lse, int32_t* topk_ids, void* workspace,
-               size_t workspace_bytes, wi_stream_t stream, int stages, bool need_q, bool need_kv) {
+               size_t workspace_bytes, wi_stream_t stream, int stages, bool need_q, bool need_kv,
+               const wi_decode_options* opt = nullptr) {
   if ((stages & wi::kStageAttend) && out == nullptr) return WI_ERR_INVALID_ARG;
   DecodeArgs a;
-  const int st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_q,
-                                  need_kv);
+  int st = check_options(opt, p);
   if (st != WI_OK) return st;
+  st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_q, need_kv);
+  if (st != WI_OK) return st;
+  if (opt != nullptr) {
+    a.rank_mass = opt->rank == WI_RANK_MASS ? 1 : 0;
+    if (opt->prev_q != nullptr && p->r > 0) {
+      a.prev_q = static_cast<const uint16_t*>(opt->prev_q);
+      a.prev_topk = opt->prev_topk;
+      a.tau = opt->tau;
+    }
+    a.reused = opt->reused;
+  }
   a.stages = stages;
   a.fused = stages == (wi::kStageScore | wi::kStageSelect | wi::kStageAttend) ? 1 : 0;
   a.out = out;
@@ -519,6 +542,14 @@ int wi_decode_attention(const wi_decode_params* p, const void* q, const void* K,
                         void* workspace, size_t workspace_bytes, wi_stream_t stream) {
   return run_decode(p, q, K, V, index, out, lse, topk_ids, workspace, workspace_bytes, stream,
                     wi::kStageScore | wi::kStageSelect | wi::kStageAttend, true, true);
+}
+
+int wi_decode_attention_ex(const wi_decode_params* p, const wi_decode_options* options,
+                           const void* q, const void* K, const void* V, const wi_index* index,
+                           float* out, float* lse, int32_t* topk_ids, void* workspace,
+                           size_t workspace_bytes, wi_stream_t stream) {
+  return run_decode(p, q, K, V, index, out, lse, topk_ids, workspace, workspace_bytes, stream,
+                    wi::kStageScore | wi::kStageSelect | wi::kStageAttend, true, true, options);
 }
 
 int wi_sync_status(void* workspace, wi_stream_t stream, int* device_status) {

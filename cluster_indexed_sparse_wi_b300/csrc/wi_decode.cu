@@ -132,6 +132,7 @@ struct __align__(128) DecSmem {
       unsigned long long cand[kCand];
       int ncand;
       int res[4];
+      float cosv[8];  // query cosines of the group (speculative reuse)
     } sel;
     struct {
       int rb[kMaxBlocks];  // blocks holding a retrieval piece of the head
@@ -148,7 +149,7 @@ struct __align__(128) DecSmem {
   unsigned static_w[kMaxBlocks];  // copy of the blocks' static work
   unsigned slot_cnt[kSlots];
   int2 scan[2][kCW];
-  uint32_t red_u[4][kCW];
+  uint32_t red_u[6][kCW];
   float red_f[2][kCW];
   int abort;      // some wait of this block gave up
   int issued;     // tiles whose copies the producer issued
@@ -190,6 +191,9 @@ __device__ __forceinline__ bool cany(bool x) {
 }
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ uint2 lds2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float4 bf4(uint2 w) {
+  return make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+}
 __device__ __forceinline__ uint32_t score_key(float s) {
   return (s == -INFINITY) ? 0u : float_key(s);  // 0 <=> empty cluster
 }
@@ -373,10 +377,17 @@ __device__ void combine_write(DecSmem& S, const float (&m)[NH], const float (&l)
 // ---------------------------------------------------------------------------
 // selection of one query head (all 512 consumers)
 // ---------------------------------------------------------------------------
-// T = the r_eff = min(r, non-empty) largest scores, ties to the lower id.
-// Keys are order-preserving images of the scores (0 = empty cluster).  The
-// keys of the first 8192 clusters are kept in shared memory (thread t holds
-// ids 16 t .. 16 t + 15); the rest are re-read from the scores at every pass.
+// T = the r_eff = min(r, non-empty) largest ranking keys, ties to the lower
+// id.  The ranking key is the score s_c, or with a.rank_mass the estimated
+// attention mass n_c e^{s_c}, compared as s_c + ln n_c (the attention-aware
+// index of technical summary (ar) §2.a).  Keys are order-preserving images of
+// these values (0 = empty cluster).  The keys of the first 8192 clusters are
+// kept in shared memory (thread t holds ids 16 t .. 16 t + 15); the rest are
+// re-read from the scores at every pass.
+//   0. speculative reuse (FreeKV technical summary §2.A): with a.prev_q set,
+//      the group's smallest cosine between a query and its previous query;
+//      if it is at least a.tau, T is the previous step's set for this head
+//      (a.prev_topk row) and steps 1-3 are skipped;
 //   1. count, smallest and largest key;
 //   2. a histogram of 1024 bins linear in the score between the smallest and
 //      largest score (monotone in the score, so few keys share a bin) gives
@@ -399,9 +410,12 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const int* sz = a.size + (size_t)bg * C;
   const int* off = a.offset + (size_t)bg * (C + 1);
   const int nch = (C + kSelChunk - 1) / kSelChunk;
-  const bool vec = (C & 3) == 0;  // rows of scores start on 16-byte boundaries
+  const bool vec = (C & 3) == 0;  // rows of scores and sizes start on 16-byte boundaries
+  const bool mass = a.rank_mass != 0;
   int buf = 0;
 
+  // ranking key of the mass order: s_c + ln n_c (0 for an empty cluster)
+  auto mass_key = [](float sv, int n) { return n > 0 ? score_key(sv + logf((float)n)) : 0u; };
   // keys of chunk ch for this thread, in groups of four: f(key, id)
   auto chunk_keys = [&](int ch, auto&& f) {
     const int c0 = ch * kSelChunk + tid * 16;
@@ -410,16 +424,37 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       float4 v[4];  // all four loads in flight before any key is used
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = __ldcg(p + j);
+      if (mass) {
+        const int4* pn = reinterpret_cast<const int4*>(sz + c0);
+        int4 n[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        f(score_key(v[j].x), c0 + 4 * j);
-        f(score_key(v[j].y), c0 + 4 * j + 1);
-        f(score_key(v[j].z), c0 + 4 * j + 2);
-        f(score_key(v[j].w), c0 + 4 * j + 3);
+        for (int j = 0; j < 4; ++j) n[j] = __ldg(pn + j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f(mass_key(v[j].x, n[j].x), c0 + 4 * j);
+          f(mass_key(v[j].y, n[j].y), c0 + 4 * j + 1);
+          f(mass_key(v[j].z, n[j].z), c0 + 4 * j + 2);
+          f(mass_key(v[j].w, n[j].w), c0 + 4 * j + 3);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f(score_key(v[j].x), c0 + 4 * j);
+          f(score_key(v[j].y), c0 + 4 * j + 1);
+          f(score_key(v[j].z), c0 + 4 * j + 2);
+          f(score_key(v[j].w), c0 + 4 * j + 3);
+        }
       }
     } else {
 #pragma unroll 4
-      for (int j = 0; j < 16; ++j) f((c0 + j < C) ? score_key(__ldcg(sc + c0 + j)) : 0u, c0 + j);
+      for (int j = 0; j < 16; ++j) {
+        uint32_t k = 0u;
+        if (c0 + j < C) {
+          const float sv = __ldcg(sc + c0 + j);
+          k = mass ? mass_key(sv, __ldg(sz + c0 + j)) : score_key(sv);
+        }
+        f(k, c0 + j);
+      }
     }
   };
   // f(key, id) over every key: chunk 0 from shared memory
@@ -428,59 +463,122 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     for (int j = 0; j < 16; ++j) f(S.u.sel.key[j][tid], tid * 16 + j);
     for (int ch = 1; ch < nch; ++ch) chunk_keys(ch, f);
   };
-  // block sum and key extrema (one barrier)
-  auto block_count_range = [&](int& cnt, uint32_t& kmx, uint32_t& kmn) {
+  // block sum, key extrema and a second maximum (one barrier)
+  auto block_count_range = [&](int& cnt, uint32_t& kmx, uint32_t& kmn, uint32_t& mx2) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       cnt += __shfl_xor_sync(kFull, cnt, o);
       kmx = max(kmx, __shfl_xor_sync(kFull, kmx, o));
       kmn = min(kmn, __shfl_xor_sync(kFull, kmn, o));
+      mx2 = max(mx2, __shfl_xor_sync(kFull, mx2, o));
     }
     int2* sh = S.scan[buf];
-    uint32_t(*ru)[kCW] = buf ? &S.red_u[2] : &S.red_u[0];
+    uint32_t(*ru)[kCW] = buf ? &S.red_u[3] : &S.red_u[0];
     buf ^= 1;
     if (lane == 0) {
       sh[warp] = make_int2(cnt, 0);
       ru[0][warp] = kmx;
       ru[1][warp] = kmn;
+      ru[2][warp] = mx2;
     }
     csync();
     cnt = 0;
     kmx = 0u;
     kmn = 0xffffffffu;
+    mx2 = 0u;
 #pragma unroll
     for (int w = 0; w < kCW; ++w) {
       cnt += sh[w].x;
       kmx = max(kmx, ru[0][w]);
       kmn = min(kmn, ru[1][w]);
+      mx2 = max(mx2, ru[2][w]);
     }
   };
 
-  // 1. keys of the first chunk into shared memory; count and key range
+  const int rsel0 = bh * rs;
+  int* ids = a.sel_ids + rsel0;
+
+  // 0. speculative reuse: the group's smallest query cosine against tau
+  bool reuse = false;
+  int n_reuse = 0;
+  if (a.prev_q != nullptr && r > 0) {
+    if (warp < a.G) {
+      const size_t row = ((size_t)bg * a.G + warp) * kD + lane * 4;
+      const float4 x = bf4(__ldg(reinterpret_cast<const uint2*>(a.q + row)));
+      const float4 y = bf4(__ldg(reinterpret_cast<const uint2*>(a.prev_q + row)));
+      float dot = x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+      float xx = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+      float yy = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        dot += __shfl_xor_sync(kFull, dot, o);
+        xx += __shfl_xor_sync(kFull, xx, o);
+        yy += __shfl_xor_sync(kFull, yy, o);
+      }
+      if (lane == 0)
+        S.u.sel.cosv[warp] = (xx > 0.f && yy > 0.f) ? dot / (sqrtf(xx) * sqrtf(yy)) : 0.f;
+    }
+    csync();
+    float cmin = S.u.sel.cosv[0];
+    for (int h = 1; h < a.G; ++h) cmin = fminf(cmin, S.u.sel.cosv[h]);
+    if (cmin >= a.tau) {
+      // the previous row: strictly ascending ids in [0, C), then -1 padding
+      const int* prv = a.prev_topk + (size_t)bh * r;
+      int n = 0, bad = 0;
+      for (int i = tid; i < r; i += kCT) {
+        const int x = __ldcg(prv + i);
+        if (x >= 0) {
+          const int y = i > 0 ? __ldcg(prv + i - 1) : -1;
+          bad |= (int)(x >= C || (i > 0 && (y < 0 || y >= x)));
+          ids[i] = x;
+          ++n;
+        } else {
+          bad |= (int)(x != -1);
+        }
+      }
+      int2 tot;
+      cscan2(make_int2(n, bad), S, &tot, buf);
+      if (tot.y != 0) {
+        if (tid == 0) report(a.status, WI_ERR_INVALID_ARG);  // not a retrieval set: select
+      } else {
+        reuse = true;
+        n_reuse = tot.x;
+      }
+    }
+  }
+  if (tid == 0 && a.reused != nullptr) a.reused[bh] = reuse ? 1 : 0;
+
+  // 1. keys of the first chunk into shared memory; count and key range; the
+  // largest score (the head's maximum) separately when the keys are not the
+  // scores or are not visited
   int valid = 0;
-  uint32_t kmax = 0u, kmin = 0xffffffffu;
+  uint32_t kmax = 0u, kmin = 0xffffffffu, smax = 0u;
   auto tally = [&](uint32_t k, int) {
     valid += (int)(k != 0u);
     kmax = max(kmax, k);
     kmin = min(kmin, k != 0u ? k : 0xffffffffu);
   };
-  {
-    int j = 0;
+  if (reuse || mass) {
+    for (int c = tid; c < C; c += kCT) smax = max(smax, score_key(__ldcg(sc + c)));
+  }
+  if (!reuse) {
     chunk_keys(0, [&](uint32_t k, int id) {
       S.u.sel.key[id - tid * 16][tid] = k;
       tally(k, id);
-      ++j;
     });
+    for (int ch = 1; ch < nch; ++ch) chunk_keys(ch, tally);
+    if (!mass) smax = kmax;
   }
-  for (int ch = 1; ch < nch; ++ch) chunk_keys(ch, tally);
-  block_count_range(valid, kmax, kmin);
-  const int r_eff = min(r, valid);
-  if (tid == 0) a.head_max[bh] = valid > 0 ? key_float(kmax) : -INFINITY;
+  block_count_range(valid, kmax, kmin, smax);
+  const int r_eff = reuse ? n_reuse : min(r, valid);
+  if (tid == 0) a.head_max[bh] = smax != 0u ? key_float(smax) : -INFINITY;
 
   // threshold (Kb, cb): selected iff k > Kb, or k == Kb and id <= cb
   uint32_t Kb = 0xffffffffu;
   int cb = -1;
-  if (r_eff > 0 && r_eff == valid) {
+  if (reuse) {
+    // T is the previous set, already in ids
+  } else if (r_eff > 0 && r_eff == valid) {
     Kb = 0u;  // every non-empty cluster
     cb = INT_MAX;
   } else if (r_eff > 0) {
@@ -551,14 +649,14 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       // 3'. a crowded bin (ties or a pathological spread): its key range, then
       // histograms of that range, kBins equal bins at a time
       int nb2 = 0;
-      uint32_t lo = 0xffffffffu, hi = 0u;
+      uint32_t lo = 0xffffffffu, hi = 0u, unused = 0u;
       visit([&](uint32_t k, int) {
         if (k != 0u && bin_of(k) == bstar) {
           lo = min(lo, k);
           hi = max(hi, k);
         }
       });
-      block_count_range(nb2, hi, lo);
+      block_count_range(nb2, hi, lo, unused);
       uint32_t span = hi - lo;
       for (int iter = 0; iter < 8; ++iter) {
         int shift = 0;
@@ -623,15 +721,13 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   }
 
   // 4. ids in ascending order, then each selected cluster's size, row, score
-  const int rsel0 = bh * rs;
-  int* ids = a.sel_ids + rsel0;
   int* rows = a.sel_rows + rsel0;
   int* cnts = a.sel_cnts + rsel0;
   int* pre = a.sel_pre + rsel0;
   float* ssel = a.sel_sc + rsel0;
   int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
   int sel_base = 0;
-  if (r_eff > 0) {
+  if (r_eff > 0 && !reuse) {
     for (int ch = 0; ch < nch; ++ch) {
       uint32_t mask = 0u;
       int nsel = 0;
@@ -662,7 +758,7 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       }
     }
   }
-  const int nsel_tot = min(sel_base, r);  // == r_eff
+  const int nsel_tot = reuse ? r_eff : min(sel_base, r);  // == r_eff
   csync();  // the ids are written (and visible to the block)
   int tok_base = 0;
   for (int i0 = 0; i0 < nsel_tot; i0 += kCT) {
@@ -671,6 +767,7 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     float sv = -INFINITY;
     if (i < nsel_tot) {
       const int c = ids[i];
+      if (reuse && topk) topk[i] = c;
       n = __ldg(sz + c);
       row = __ldg(off + c);
       sv = __ldcg(sc + c);
@@ -1235,10 +1332,6 @@ __device__ void heads_flush(DecSmem& S, HeadsState<G>& e, float* base, int lane)
 template <int G>
 __device__ __noinline__ void heads_flush_nv(DecSmem& S, HeadsState<G> e, float* base) {
   heads_flush<G>(S, e, base, threadIdx.x & 31);
-}
-
-__device__ __forceinline__ float4 bf4(uint2 w) {
-  return make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
 }
 
 // ---------------------------------------------------------------------------

@@ -95,6 +95,12 @@ struct DecodeArgs {
   int nchunks;          // ceil(nt / Q); chunk j is taken by block j % nb in round j / nb
   int rounds;           // ceil(nchunks / nb)
   int inject;           // test hook: every block skips the copies of its first tile
+  // selection options
+  int rank_mass;        // rank clusters by s_c + ln n_c instead of s_c
+  float tau;            // reuse threshold on the group's smallest query cosine
+  const uint16_t* prev_q;  // bf16 [B,Hq,128] previous step's queries, or null (no reuse)
+  const int* prev_topk;    // [B,Hq,r] previous step's retrieved ids (ascending, -1 padding)
+  int* reused;             // [B,Hkv] 1 where the group reused, or null
   long long static_units;         // sum of static_w
   unsigned static_w[kMaxBlocks];  // static work of each block, 4 KB units
   // outputs

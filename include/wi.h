@@ -238,6 +238,46 @@ WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const v
                         const wi_index *index, float *out, float *lse, int32_t *topk_ids,
                         void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
+/* Ranking keys of the retrieval zone (wi_decode_options.rank). */
+enum { WI_RANK_SCORE = 0, WI_RANK_MASS = 1 };
+
+/* Options of wi_decode_attention_ex.  All-zero options (rank WI_RANK_SCORE,
+ * prev_q NULL, reused NULL) give wi_decode_attention. */
+typedef struct {
+  /* WI_RANK_SCORE: T = the r largest s_c (ties to the lower id).
+   * WI_RANK_MASS: T = the r largest estimated attention masses n_c e^{s_c},
+   * compared as s_c + ln n_c in f32 (ties to the lower id); the attention-
+   * aware ranking of technical summary (ar) §2.a.  Everything after the
+   * selection is unchanged. */
+  int rank;
+  /* Speculative reuse with correction (FreeKV technical summary §2.A).  With
+   * prev_q set, for each KV group (b, g) the smallest cosine
+   * cos(q[b,h], prev_q[b,h]) over its query heads h (0 where either query is
+   * zero; f32) is compared with tau: if it is >= tau, every head of the group
+   * takes as T the ids of its row of prev_topk instead of selecting; else
+   * the group selects afresh.  The decision is an f32 comparison: a cosine
+   * within rounding of tau may go either way.  A prev_topk row must hold
+   * strictly ascending ids in [0, C) followed by -1 padding (what topk_ids
+   * returns); a row that does not is reported as WI_ERR_INVALID_ARG in the
+   * device status and that head selects afresh.  topk_ids may be the same
+   * array as prev_topk: each row is read before it is rewritten.  Ignored
+   * when r = 0. */
+  float tau;
+  const void *prev_q;        /* bf16 [B,Hq,d] device, 16-byte aligned, or NULL   */
+  const int32_t *prev_topk;  /* i32 [B,Hq,r] device (required with prev_q)      */
+  int32_t *reused;           /* i32 [B,Hq] device or NULL: 1 where the head took
+                                its previous set, else 0                         */
+} wi_decode_options;
+
+/* wi_decode_attention with selection options (options may be NULL).
+ * Returns WI_ERR_INVALID_ARG for an unknown rank, prev_q without prev_topk
+ * or a NaN tau, and WI_ERR_ALIGNMENT for misaligned option pointers, before
+ * anything is enqueued. */
+WI_API int wi_decode_attention_ex(const wi_decode_params *p, const wi_decode_options *options,
+                           const void *q, const void *K, const void *V,
+                           const wi_index *index, float *out, float *lse, int32_t *topk_ids,
+                           void *workspace, size_t workspace_bytes, wi_stream_t stream);
+
 /* Decode stage 1: one stream over the centroid keys and the value sums:
  * the cluster scores s into the workspace, and the estimate of every
  * non-empty cluster, (m, l = sum n_c e^{s_c - m}, o = sum e^{s_c - m}

@@ -172,3 +172,34 @@ def test_decode_index_mismatch_and_workspace(L):
     assert lib.wi_decode_attention(ctypes.byref(dp(L)), fake, fake, fake, ctypes.byref(ix), fake,
                                    None, None, ctypes.c_void_p((1 << 20) + 16), 1 << 30,
                                    None) == L.WI_ERR_ALIGNMENT
+
+
+def test_decode_option_validation(L):
+    # the options are checked before anything else of the call
+    lib = L.lib()
+    ix = L.IndexStruct()
+    for name in L.FIELDS:
+        setattr(ix, name, 1 << 20)
+    ix.B, ix.Hkv, ix.N, ix.d, ix.sink, ix.window, ix.n_clusters = 1, 2, 4096, 128, 4, 64, 256
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(**kw):
+        o = L.DecodeOptions()
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return lib.wi_decode_attention_ex(ctypes.byref(dp(L)), ctypes.byref(o), fake, fake, fake,
+                                          ctypes.byref(ix), fake, None, None, fake, 1 << 30, None)
+
+    assert call(rank=2) == L.WI_ERR_INVALID_ARG
+    assert call(rank=-1) == L.WI_ERR_INVALID_ARG
+    assert call(prev_q=1 << 20) == L.WI_ERR_INVALID_ARG              # no prev_topk
+    assert call(prev_q=1 << 20, prev_topk=1 << 20, tau=float("nan")) == L.WI_ERR_INVALID_ARG
+    assert call(prev_q=(1 << 20) + 8, prev_topk=1 << 20) == L.WI_ERR_ALIGNMENT
+    assert call(prev_q=1 << 20, prev_topk=(1 << 20) + 2) == L.WI_ERR_ALIGNMENT
+    assert call(rank=1, reused=(1 << 20) + 1) == L.WI_ERR_ALIGNMENT
+    # valid options reach the remaining checks (here the index mismatch)
+    ix.window = 32
+    assert call(rank=1, prev_q=1 << 20, prev_topk=1 << 20, tau=0.5) == L.WI_ERR_INDEX_MISMATCH
+    assert lib.wi_decode_attention_ex(ctypes.byref(dp(L)), None, fake, fake, fake,
+                                      ctypes.byref(ix), fake, None, None, fake, 1 << 30,
+                                      None) == L.WI_ERR_INDEX_MISMATCH
