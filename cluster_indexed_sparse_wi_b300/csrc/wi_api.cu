@@ -364,6 +364,12 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   const int nst = (int)groups * d.tph;
   for (int t = 0; t < nst; ++t) a->static_w[wi::steady_block(*a, t)] += 8u;
   for (size_t bh = 0; bh < heads; ++bh) a->static_w[wi::sel_block(*a, (int)bh)] += su;
+  // Retrieval starts once every selection is published: after the centroid-
+  // key tiles of the last round (the value-sum tiles of the earlier rounds
+  // interleaved) and one selection.  Work a block finishes before then does
+  // not delay its retrieval share, so only the rest counts.
+  const unsigned wait = 8u * (unsigned)d.Q * (2u * (unsigned)d.rounds - 1u) + su;
+  for (int b = 0; b < nb; ++b) a->static_w[b] = a->static_w[b] > wait ? a->static_w[b] - wait : 0u;
   a->static_units = 0;
   for (int b = 0; b < nb; ++b) a->static_units += a->static_w[b];
   return WI_OK;

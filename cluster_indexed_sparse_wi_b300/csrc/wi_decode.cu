@@ -375,6 +375,253 @@ __device__ void combine_write(DecSmem& S, const float (&m)[NH], const float (&l)
 }
 
 // ---------------------------------------------------------------------------
+// selection of one query head, common case (all 512 consumers)
+// ---------------------------------------------------------------------------
+// The same set as the general path below, in three passes over the ranking
+// values v (the score, or s_c + ln n_c; -inf = empty cluster).  Thread t holds
+// the values of ids 16 t .. 16 t + 15 of the first 8192 clusters in
+// registers; further clusters are re-read at every pass.
+//   A. count, smallest and largest value (and the largest score);
+//   B. a histogram of kBins bins linear in v between them (monotone in v);
+//      a scan from the top gives the bin b* holding the r_eff-th largest;
+//   C. ids in bins above b* are marked in a bitmap of the ids; b*'s values
+//      are ranked exactly by (v desc, id asc) and the best `need` marked;
+//   then the bitmap, read in id order, gives the ids in ascending order.
+// Returns the number selected, or -1 (nothing written) when b* holds more
+// than kCand values or the ids do not fit the bitmap: the general path then
+// takes over.
+__device__ int select_fast(const DecodeArgs& a, DecSmem& S, int bh, int* ids, int* topk) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bg = bh / a.G;
+  const int C = a.C, r = a.r;
+  const float* sc = a.scores + (size_t)bh * C;
+  const int* sz = a.size + (size_t)bg * C;
+  const int nch = (C + kSelChunk - 1) / kSelChunk;
+  const int nwords = (C + 31) / 32;
+  if (nwords > 16 * kCT) return -1;  // the bitmap lives in S.u.sel.key
+  uint32_t* bits = &S.u.sel.key[0][0];
+  const bool vec = (C & 3) == 0;
+  const bool mass = a.rank_mass != 0;
+  float smx = -INFINITY;  // largest score (differs from the largest v when ranking by mass)
+  auto mval = [](float s, int n) { return n > 0 ? s + logf((float)n) : -INFINITY; };
+  // values of chunk ch for this thread
+  auto load = [&](int ch, float (&x)[16]) {
+    const int c0 = ch * kSelChunk + tid * 16;
+    if (vec && c0 + 16 <= C) {
+      const float4* p = reinterpret_cast<const float4*>(sc + c0);
+      float4 f[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = __ldcg(p + j);
+      if (mass) {
+        const int4* pn = reinterpret_cast<const int4*>(sz + c0);
+        int4 n[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) n[j] = __ldg(pn + j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          smx = fmaxf(smx, fmaxf(fmaxf(f[j].x, f[j].y), fmaxf(f[j].z, f[j].w)));
+          x[4 * j] = mval(f[j].x, n[j].x);
+          x[4 * j + 1] = mval(f[j].y, n[j].y);
+          x[4 * j + 2] = mval(f[j].z, n[j].z);
+          x[4 * j + 3] = mval(f[j].w, n[j].w);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[4 * j] = f[j].x;
+          x[4 * j + 1] = f[j].y;
+          x[4 * j + 2] = f[j].z;
+          x[4 * j + 3] = f[j].w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        x[j] = -INFINITY;
+        if (c0 + j < C) {
+          const float s = __ldcg(sc + c0 + j);
+          smx = fmaxf(smx, s);
+          x[j] = mass ? mval(s, __ldg(sz + c0 + j)) : s;
+        }
+      }
+    }
+  };
+  // lean block scan: exclusive prefix and total of x over the 512 consumers
+  auto bscan = [&](int x, int2* sh, int& total) {
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh[warp].x = incl;
+    csync();
+    const int wt = sh[lane & (kCW - 1)].x;
+    int wincl = wt;
+#pragma unroll
+    for (int o = 1; o < kCW; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, wincl, o);
+      if ((lane & (kCW - 1)) >= o) wincl += y;
+    }
+    total = __shfl_sync(kFull, wincl, kCW - 1);
+    return __shfl_sync(kFull, wincl - wt, warp) + incl - x;
+  };
+
+  // A. count and range; the histogram and the bitmap are cleared meanwhile
+  float v[16];
+  load(0, v);
+  int cnt = 0;
+  float vmax = -INFINITY, vmin = INFINITY;
+  auto tally = [&](const float (&x)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const bool ok = x[j] > -INFINITY;
+      cnt += (int)ok;
+      vmax = ok ? fmaxf(vmax, x[j]) : vmax;
+      vmin = ok ? fminf(vmin, x[j]) : vmin;
+    }
+  };
+  tally(v);
+  for (int ch = 1; ch < nch; ++ch) {
+    float x[16];
+    load(ch, x);
+    tally(x);
+  }
+  if (!mass) smx = vmax;
+  for (int i = tid; i < kBins; i += kCT) S.u.sel.hist[i] = 0;
+  for (int i = tid; i < nwords; i += kCT) bits[i] = 0u;
+  if (tid == 0) S.u.sel.ncand = 0;
+  {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cnt += __shfl_xor_sync(kFull, cnt, o);
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
+      vmin = fminf(vmin, __shfl_xor_sync(kFull, vmin, o));
+      smx = fmaxf(smx, __shfl_xor_sync(kFull, smx, o));
+    }
+    if (lane == 0) {
+      S.red_u[0][warp] = (uint32_t)cnt;
+      S.red_u[1][warp] = __float_as_uint(vmax);
+      S.red_u[2][warp] = __float_as_uint(vmin);
+      S.red_u[3][warp] = __float_as_uint(smx);
+    }
+    csync();
+    const int w = lane & (kCW - 1);
+    cnt = (int)S.red_u[0][w];
+    vmax = __uint_as_float(S.red_u[1][w]);
+    vmin = __uint_as_float(S.red_u[2][w]);
+    smx = __uint_as_float(S.red_u[3][w]);
+#pragma unroll
+    for (int o = kCW / 2; o > 0; o >>= 1) {
+      cnt += __shfl_xor_sync(kFull, cnt, o);
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
+      vmin = fminf(vmin, __shfl_xor_sync(kFull, vmin, o));
+      smx = fmaxf(smx, __shfl_xor_sync(kFull, smx, o));
+    }
+  }
+  const int r_eff = min(r, cnt);
+  if (tid == 0) a.head_max[bh] = cnt > 0 ? smx : -INFINITY;
+  if (r_eff == 0) return 0;
+
+  // B. histogram and boundary bin (skipped when every valid id is taken)
+  const float inv = (vmax > vmin) ? (float)kBins / (vmax - vmin) : 0.f;
+  auto binf = [&](float x) { return min((int)((x - vmin) * inv), kBins - 1); };
+  int bstar = -1, need = 0;
+  if (r_eff < cnt) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (v[j] > -INFINITY) atomicAdd(&S.u.sel.hist[binf(v[j])], 1);
+    for (int ch = 1; ch < nch; ++ch) {
+      float x[16];
+      load(ch, x);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (x[j] > -INFINITY) atomicAdd(&S.u.sel.hist[binf(x[j])], 1);
+    }
+    csync();
+    // thread t owns bins kBins-1-2t and kBins-2-2t (counted from the top)
+    const int b_hi = kBins - 1 - 2 * tid;
+    const int c1 = S.u.sel.hist[b_hi], c2 = S.u.sel.hist[b_hi - 1];
+    int tot;
+    const int above = bscan(c1 + c2, S.scan[0], tot);
+    if (above < r_eff && r_eff <= above + c1) {
+      S.u.sel.res[0] = b_hi;
+      S.u.sel.res[1] = r_eff - above;
+      S.u.sel.res[2] = c1;
+    } else if (above + c1 < r_eff && r_eff <= above + c1 + c2) {
+      S.u.sel.res[0] = b_hi - 1;
+      S.u.sel.res[1] = r_eff - above - c1;
+      S.u.sel.res[2] = c2;
+    }
+    csync();
+    bstar = S.u.sel.res[0];
+    need = S.u.sel.res[1];
+    if (S.u.sel.res[2] > kCand) return -1;  // crowded bin: the general path
+  }
+
+  // C. mark the ids above b*, collect b*'s values (every valid id when bstar < 0)
+  auto mark = [&](int ch, const float (&x)[16]) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (!(x[j] > -INFINITY)) continue;
+      const int b = bstar < 0 ? kBins : binf(x[j]);
+      if (b > bstar) {
+        m |= 1u << j;
+      } else if (b == bstar) {
+        const int p = atomicAdd(&S.u.sel.ncand, 1);  // p < kCand: the bin holds <= kCand
+        const uint32_t id = (uint32_t)(ch * kSelChunk + tid * 16 + j);
+        S.u.sel.cand[p] = ((unsigned long long)score_key(x[j]) << 32) |
+                          (unsigned long long)(0xffffffffu - id);
+      }
+    }
+    if (m) atomicOr(&bits[ch * (kSelChunk / 32) + (tid >> 1)], m << ((tid & 1) * 16));
+  };
+  mark(0, v);
+  for (int ch = 1; ch < nch; ++ch) {
+    float x[16];
+    load(ch, x);
+    mark(ch, x);
+  }
+  csync();
+  if (bstar >= 0) {
+    // the best `need` of b*'s values: ranked by (value desc, id asc)
+    const int nc = S.u.sel.ncand;
+    if (tid < nc) {
+      const unsigned long long mine = S.u.sel.cand[tid];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += (int)(S.u.sel.cand[j] > mine);
+      if (rank < need) {
+        const uint32_t id = 0xffffffffu - (uint32_t)mine;
+        atomicOr(&bits[id >> 5], 1u << (id & 31));
+      }
+    }
+    csync();
+  }
+
+  // the marked ids in ascending order: thread t reads words [t k, t k + k)
+  const int kw = (nwords + kCT - 1) / kCT;
+  const int w0 = tid * kw, w1 = min(w0 + kw, nwords);
+  int n = 0;
+  for (int w = w0; w < w1; ++w) n += __popc(bits[w]);
+  int tot;
+  int pos = bscan(n, S.scan[1], tot);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t m = bits[w];
+    while (m) {
+      const int id = w * 32 + __ffs(m) - 1;
+      m &= m - 1;
+      if (pos < r) {
+        ids[pos] = id;
+        if (topk) topk[pos] = id;
+      }
+      ++pos;
+    }
+  }
+  return min(tot, r);  // == r_eff
+}
+
+// ---------------------------------------------------------------------------
 // selection of one query head (all 512 consumers)
 // ---------------------------------------------------------------------------
 // T = the r_eff = min(r, non-empty) largest ranking keys, ties to the lower
@@ -401,6 +648,7 @@ __device__ void combine_write(DecSmem& S, const float (&m)[NH], const float (&l)
 //   4. the selected ids are written in id order; then every selected
 //      cluster's size, first sorted row and score are loaded in one round and
 //      a scan of the sizes gives the token offsets.
+// Steps 1-3 and the marking of step 4 run only when select_fast gives up.
 // Returns the number selected.
 __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -547,6 +795,9 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     }
   }
   if (tid == 0 && a.reused != nullptr) a.reused[bh] = reuse ? 1 : 0;
+  int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
+  const int n_fast = reuse ? -1 : select_fast(a, S, bh, ids, topk);
+  const bool general = !reuse && n_fast < 0;
 
   // 1. keys of the first chunk into shared memory; count and key range; the
   // largest score (the head's maximum) separately when the keys are not the
@@ -558,10 +809,10 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     kmax = max(kmax, k);
     kmin = min(kmin, k != 0u ? k : 0xffffffffu);
   };
-  if (reuse || mass) {
+  if (reuse || (general && mass)) {
     for (int c = tid; c < C; c += kCT) smax = max(smax, score_key(__ldcg(sc + c)));
   }
-  if (!reuse) {
+  if (general) {
     chunk_keys(0, [&](uint32_t k, int id) {
       S.u.sel.key[id - tid * 16][tid] = k;
       tally(k, id);
@@ -569,15 +820,17 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     for (int ch = 1; ch < nch; ++ch) chunk_keys(ch, tally);
     if (!mass) smax = kmax;
   }
-  block_count_range(valid, kmax, kmin, smax);
-  const int r_eff = reuse ? n_reuse : min(r, valid);
-  if (tid == 0) a.head_max[bh] = smax != 0u ? key_float(smax) : -INFINITY;
+  if (reuse || general) {
+    block_count_range(valid, kmax, kmin, smax);
+    if (tid == 0) a.head_max[bh] = smax != 0u ? key_float(smax) : -INFINITY;
+  }
+  const int r_eff = reuse ? n_reuse : (general ? min(r, valid) : n_fast);
 
   // threshold (Kb, cb): selected iff k > Kb, or k == Kb and id <= cb
   uint32_t Kb = 0xffffffffu;
   int cb = -1;
-  if (reuse) {
-    // T is the previous set, already in ids
+  if (!general) {
+    // T is the previous set, or select_fast's, already in ids
   } else if (r_eff > 0 && r_eff == valid) {
     Kb = 0u;  // every non-empty cluster
     cb = INT_MAX;
@@ -725,9 +978,8 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   int* cnts = a.sel_cnts + rsel0;
   int* pre = a.sel_pre + rsel0;
   float* ssel = a.sel_sc + rsel0;
-  int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
   int sel_base = 0;
-  if (r_eff > 0 && !reuse) {
+  if (r_eff > 0 && general) {
     for (int ch = 0; ch < nch; ++ch) {
       uint32_t mask = 0u;
       int nsel = 0;
@@ -758,7 +1010,7 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       }
     }
   }
-  const int nsel_tot = reuse ? r_eff : min(sel_base, r);  // == r_eff
+  const int nsel_tot = general ? min(sel_base, r) : r_eff;  // == r_eff
   csync();  // the ids are written (and visible to the block)
   int tok_base = 0;
   for (int i0 = 0; i0 < nsel_tot; i0 += kCT) {
