@@ -356,6 +356,11 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->Q = d.Q;
   a->nchunks = d.nchunks;
   a->rounds = d.rounds;
+  // With few heads, the selections of the groups scored in the last round
+  // would start only near the end of the index stream: score every round
+  // first and select in one wave.  With many heads, selections round by
+  // round keep the index stream busy on the other blocks meanwhile.
+  a->kbar_first = (d.rounds > 1 && (long long)p->B * p->Hq <= nb) ? 1 : 0;
   // static work of every block (4 KB units): its index tiles (centroid keys
   // and value sums, 64 KB per tile), steady tiles (32 KB) and selections
   const unsigned su = selection_units(C);
@@ -365,10 +370,11 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   for (int t = 0; t < nst; ++t) a->static_w[wi::steady_block(*a, t)] += 8u;
   for (size_t bh = 0; bh < heads; ++bh) a->static_w[wi::sel_block(*a, (int)bh)] += su;
   // Retrieval starts once every selection is published: after the centroid-
-  // key tiles of the last round (the value-sum tiles of the earlier rounds
-  // interleaved) and one selection.  Work a block finishes before then does
-  // not delay its retrieval share, so only the rest counts.
-  const unsigned wait = 8u * (unsigned)d.Q * (2u * (unsigned)d.rounds - 1u) + su;
+  // key tiles of every round (and, round by round, the value-sum tiles of
+  // the earlier rounds) and one selection.  Work a block finishes before
+  // then does not delay its retrieval share, so only the rest counts.
+  const unsigned wait =
+      8u * (unsigned)d.Q * (a->kbar_first ? (unsigned)d.rounds : 2u * (unsigned)d.rounds - 1u) + su;
   for (int b = 0; b < nb; ++b) a->static_w[b] = a->static_w[b] > wait ? a->static_w[b] - wait : 0u;
   a->static_units = 0;
   for (int b = 0; b < nb; ++b) a->static_units += a->static_w[b];

@@ -1243,11 +1243,18 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
     bool ok = true;
     const bool side_bulk = (a.C & 3) == 0;  // rows of sizes start 16-byte aligned
     if (a.stages & kStageScore) {
-      for (int rd = 0; rd < a.rounds && ok; ++rd) {
-        const int j = rd * a.nb + (int)blockIdx.x;
-        if (j >= a.nchunks) break;
-        const int n = chunk_tiles(a, j);
-        for (int pass = 0; pass < 2 && ok; ++pass) {
+      // round by round, centroid-key tiles then value-sum tiles; or, with
+      // a.kbar_first, every round's centroid-key tiles, then every round's
+      // value-sum tiles in reverse round order (the consumers still hold the
+      // last round's scores in shared memory)
+      {
+        for (int step = 0; step < 2 * a.rounds && ok; ++step) {
+          const int pass = a.kbar_first ? step / a.rounds : step & 1;
+          const int rd = !a.kbar_first ? step >> 1
+                         : (pass == 0 ? step : 2 * a.rounds - 1 - step);
+          const int j = rd * a.nb + (int)blockIdx.x;
+          if (j >= a.nchunks) continue;
+          const int n = chunk_tiles(a, j);
           const float* src = pass == 0 ? a.kbar : a.vsum;
           int bg = (j * a.Q) / a.tpg, c0 = (j * a.Q - bg * a.tpg) * kTile;
           int q_bg = -1;  // the group whose query rows were staged last
@@ -1746,10 +1753,27 @@ __device__ __forceinline__ void selections(const DecodeArgs& a, DecSmem& S, cons
 // against the warp's own maximum score of each KV group (a fixed reference:
 // no rescaling), one partial per (chunk, KV group, query head).
 template <int G>
-__device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n) {
+__device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n,
+                                           bool refill) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L4 = 4 * G;
   const int jr = lane_row<G>(lane), hr = lane_head<G>(lane);
+  if (refill) {
+    // the chunk's scores and sizes back into this warp's shared-memory slots,
+    // as its centroid-key pass left them (-inf / 0 past the group's last row)
+    if (lane < L4) {
+      for (int i = 0; i < n; ++i) {
+        const int t = j * a.Q + i, bg = t / a.tpg;
+        const int c0 = (t - bg * a.tpg) * kTile, row = warp * 4 + jr;
+        const bool in = c0 + row < a.C;
+        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+        const float* srow = a.scores + ((size_t)b * a.Hq + (size_t)g * G + hr) * a.C;
+        S.a.chunk.sc[i][warp][lane] = in ? __ldcg(srow + c0 + row) : -INFINITY;
+        if (hr == 0) S.a.chunk.n[i][warp][jr] = in ? __ldg(a.size + (size_t)bg * a.C + c0 + row) : 0;
+      }
+    }
+    __syncwarp();
+  }
   // one KV group at a time: tiles [i0, i1) of the chunk
   for (int i0 = 0; i0 < n;) {
     const int bg = (j * a.Q + i0) / a.tpg;
@@ -2053,13 +2077,40 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S) {
   Ring rg;
   rg.seq = 0;
   rg.hollow = false;
-  // 1. index chunks, with the selections of each round between their two passes
-  for (int rd = 0; rd < a.rounds; ++rd) {
+  // 1. the centroid-key tiles of every round, the selections, then the
+  // value-sum tiles of every round, last round first (its scores are still
+  // in shared memory; earlier rounds' are read back)
+  auto chunk_n = [&](int rd) {
     const int j = rd * a.nb + blk;
-    const int n = (j < a.nchunks && (a.stages & kStageScore)) ? chunk_tiles(a, j) : 0;
-    if (n > 0) kbar_tiles<G>(a, S, rg, j, n);
-    if (a.stages & kStageSelect) selections<G>(a, S, rg, rd);
-    if (n > 0) vsum_tiles<G>(a, S, rg, j, n);
+    return (j < a.nchunks && (a.stages & kStageScore)) ? chunk_tiles(a, j) : 0;
+  };
+  // steps: (centroid-key tiles, selections, value-sum tiles) of round 0, of
+  // round 1, ...; or with a.kbar_first every round's centroid-key tiles,
+  // every round's selections, every round's value-sum tiles (last round
+  // first)
+  int last_rd = -1;
+  for (int step = 0; step < 3 * a.rounds; ++step) {
+    int kind, rd;
+    if (a.kbar_first) {
+      kind = step / a.rounds;
+      rd = step - kind * a.rounds;
+      if (kind == 2) rd = a.rounds - 1 - rd;
+    } else {
+      rd = step / 3;
+      kind = step - rd * 3;
+    }
+    if (kind == 1) {
+      if (a.stages & kStageSelect) selections<G>(a, S, rg, rd);
+      continue;
+    }
+    const int n = chunk_n(rd);
+    if (n == 0) continue;
+    if (kind == 0) {
+      kbar_tiles<G>(a, S, rg, rd * a.nb + blk, n);
+      last_rd = rd;
+    } else {
+      vsum_tiles<G>(a, S, rg, rd * a.nb + blk, n, a.kbar_first && rd != last_rd);
+    }
   }
   if (a.stages & kStageAttend) {
     steady_tiles<G>(a, S, rg);  // 2.

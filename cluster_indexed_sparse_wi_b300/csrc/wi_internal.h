@@ -94,6 +94,7 @@ struct DecodeArgs {
   int Q;                // index tiles per chunk (<= kChunkMax)
   int nchunks;          // ceil(nt / Q); chunk j is taken by block j % nb in round j / nb
   int rounds;           // ceil(nchunks / nb)
+  int kbar_first;       // every round's centroid-key tiles before any selection
   int inject;           // test hook: every block skips the copies of its first tile
   // selection options
   int rank_mass;        // rank clusters by s_c + ln n_c instead of s_c

@@ -5,9 +5,12 @@ over an index built on the GPU.  Sampled query heads are then compared with
 the oracle, which runs on the index the GPU used (downloaded for the head's
 KV group).
 
-* 128K context: 8192 clusters per head, r = 148; the fast selection path.
-* 1M context: 65536 clusters per head, r = 656; the exact radix selection
-  path.
+* 128K context: 8192 clusters per head, r = 148; one round of index tiles,
+  selection values held in registers.
+* 1M context: 65536 clusters per head, r = 656; four rounds of index tiles,
+  selection values re-read per pass.
+* 128K context, batch 16: seven rounds of index tiles (value-sum tiles of
+  earlier rounds read their scores back), heads of several sequences.
 
 Tolerances are those of test_gpu_decode:
 * cluster scores: relative 1e-5;
@@ -39,8 +42,10 @@ def gpu_head_index(ix, b, g):
             "offset": ix.offset[b, g].cpu().numpy().astype(np.int64)}
 
 
-@pytest.mark.parametrize("name,heads", [("llama3_8b_128k_b1", [0, 13, 22, 31]),
-                                        ("llama3_8b_1m_b1", [5, 30])])
+@pytest.mark.parametrize("name,heads", [
+    ("llama3_8b_128k_b1", [(0, 0), (0, 13), (0, 22), (0, 31)]),
+    ("llama3_8b_1m_b1", [(0, 5), (0, 30)]),
+    ("llama3_8b_128k_b16", [(0, 3), (7, 17), (15, 30)])])
 def test_full_size_sampled_heads(name, heads):
     import cluster_indexed_sparse_wi_b300 as wl
     w = WORKLOADS[name]
@@ -60,24 +65,24 @@ def test_full_size_sampled_heads(name, heads):
     scores = dec.scores().cpu().numpy()
     G = w.Hq // w.Hkv
     groups = {}
-    for h in heads:
+    for b, h in heads:
         gg = h // G
-        if gg not in groups:
-            groups[gg] = (wi.bf16_bits_to_f64(g["K"][0, gg]), wi.bf16_bits_to_f64(g["V"][0, gg]),
-                          gpu_head_index(ix, 0, gg))
-        Kf, Vf, hi = groups[gg]
-        qf = wi.bf16_bits_to_f64(g["q"][0, h])
+        if (b, gg) not in groups:
+            groups[(b, gg)] = (wi.bf16_bits_to_f64(g["K"][b, gg]),
+                               wi.bf16_bits_to_f64(g["V"][b, gg]), gpu_head_index(ix, b, gg))
+        Kf, Vf, hi = groups[(b, gg)]
+        qf = wi.bf16_bits_to_f64(g["q"][b, h])
         ref = wi.decode_head(qf, Kf, Vf, hi, w.sink, w.window, w.r, dec.scale)
         s_ref = ref["scores"]
         fin = np.isfinite(s_ref)
-        assert np.array_equal(np.isfinite(scores[0, h]), fin)
-        np.testing.assert_allclose(scores[0, h][fin], s_ref[fin], rtol=SCORE_TOL, atol=SCORE_TOL)
-        sel = topk[0, h][topk[0, h] >= 0]
+        assert np.array_equal(np.isfinite(scores[b, h]), fin)
+        np.testing.assert_allclose(scores[b, h][fin], s_ref[fin], rtol=SCORE_TOL, atol=SCORE_TOL)
+        sel = topk[b, h][topk[b, h] >= 0]
         assert len(sel) == min(w.r, int(fin.sum()))
         assert np.all(np.diff(sel) > 0)  # ascending ids
         assert sets_match_mod_ties(sel, ref["selected"], s_ref, SCORE_TOL)
         if set(sel.tolist()) != set(ref["selected"].tolist()):
             ref = wi.decode_head(qf, Kf, Vf, hi, w.sink, w.window, w.r, dec.scale, selected=sel)
-        e = rel_err(out[0, h], ref["out"])
-        assert e <= OUT_TOL, (name, h, e)
-        assert abs(lse[0, h] - ref["lse"]) <= LSE_TOL, (name, h, lse[0, h], ref["lse"])
+        e = rel_err(out[b, h], ref["out"])
+        assert e <= OUT_TOL, (name, b, h, e)
+        assert abs(lse[b, h] - ref["lse"]) <= LSE_TOL, (name, b, h, lse[b, h], ref["lse"])
