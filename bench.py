@@ -19,6 +19,7 @@ import hashlib
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -36,7 +37,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
@@ -52,7 +53,7 @@ def parse():
     ap.add_argument("--no-build-timing", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the 1M-context and batch-16 decode workloads")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -453,8 +454,32 @@ def gpu_uuid_str(dev):
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
+def relaunch_command(argv, n_gpus, port, python=None):
+    """The torch.distributed.run command that starts this bench once per GPU
+    (one process per GPU, rendezvous on 127.0.0.1) with the same arguments."""
+    return [python or sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            "--nproc-per-node", str(n_gpus), "--master-addr", "127.0.0.1",
+            "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
+def maybe_relaunch(args, argv, run=subprocess.call):
+    """`--gpus N` with N > 1 started as a single process: run the N ranks under
+    torch.distributed.run and return its exit status; None when this process
+    is already a rank (WORLD_SIZE set) or N == 1."""
+    if args.gpus <= 1 or "WORLD_SIZE" in os.environ:
+        return None
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return run(relaunch_command(argv, args.gpus, port))
+
+
 def main():
     args = parse()
+    rc = maybe_relaunch(args, sys.argv[1:])
+    if rc is not None:
+        return rc
     from workloads import WORKLOADS, generate, retrieval_budget
     w = WORKLOADS[args.workload]
     r = retrieval_budget(w, args.budget_frac) if args.budget_frac else w.r
@@ -628,4 +653,4 @@ def main():
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main() or 0)

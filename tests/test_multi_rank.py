@@ -47,3 +47,27 @@ def test_two_rank_replicas_and_timing_reduction():
     (r0, seeds0, k0, t0), (r1, seeds1, k1, t1) = res
     assert seeds0 != seeds1           # each rank decodes its own sequences
     assert t0 == t1 == [2.0, 10.0]    # max over ranks, seen by every rank
+
+
+def test_gpus_flag_relaunches_under_torch_distributed_run(monkeypatch):
+    # `bench.py --gpus 4` started as one process re-executes itself as four
+    # ranks (rendezvous on 127.0.0.1) with the same arguments; a rank (with
+    # WORLD_SIZE set) or --gpus 1 runs in place.
+    import bench
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    seen = []
+    args = bench.parse(["--gpus", "4", "--steps", "7", "--warmup", "3"])
+    rc = bench.maybe_relaunch(args, ["--gpus", "4", "--steps", "7", "--warmup", "3"],
+                              run=lambda cmd: seen.append(cmd) or 0)
+    assert rc == 0 and len(seen) == 1
+    cmd = seen[0]
+    i = cmd.index("-m")
+    assert cmd[i + 1] == "torch.distributed.run"
+    assert cmd[cmd.index("--nproc-per-node") + 1] == "4"
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert int(cmd[cmd.index("--master-port") + 1]) > 0
+    assert cmd[-7].endswith("bench.py") and cmd[-6:] == ["--gpus", "4", "--steps", "7", "--warmup", "3"]
+    assert bench.maybe_relaunch(bench.parse(["--gpus", "1"]), [], run=seen.append) is None
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    assert bench.maybe_relaunch(args, [], run=seen.append) is None
+    assert len(seen) == 1
