@@ -63,6 +63,8 @@ __all__ = [
     "select_clusters",
     "ranking_keys",
     "reuse_groups",
+    "round_index_bf16",
+    "group_selection",
     "decode_head",
     "decode",
 ]
@@ -317,6 +319,32 @@ def select_clusters(s: np.ndarray, r: int) -> np.ndarray:
     return np.sort(ids[finite][order][:r])
 
 
+def round_index_bf16(index: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
+    """The leaner index of the GQA-shared variant: centroid keys and value
+    sums held as bf16 (round to nearest, ties to even), which halves the
+    bytes decode streams from the index.  Reading: the pages fix no storage
+    type; the rounding is applied to the float32 index the build stores, so
+    the quantisation is decided in the precision the stored values have.
+    Sizes, offsets, perm and the sorted copies are unchanged."""
+    out = dict(index)
+    for key in ("centroid_key", "value_sum"):
+        out[key] = bf16_round(np.asarray(index[key], dtype=np.float32).astype(np.float64))
+    return out
+
+
+def group_selection(q_group: np.ndarray, centroid_key: np.ndarray, size: np.ndarray,
+                    scale: float, r: int, rank: str = "score") -> np.ndarray:
+    """GQA-shared retrieval zone: one set for all query heads of a KV head,
+    the r largest summed ranking keys sum_h key_h(c) over the group's queries
+    q_group [G, d] (ties to the lower id).  Reading: the pages leave the
+    selection granularity open; summing the heads' keys is the plainest group
+    score (for scores it is the score of the summed query)."""
+    keys = np.zeros(centroid_key.shape[0])
+    for qh in q_group:
+        keys = keys + ranking_keys(cluster_scores(qh, centroid_key, size, scale), size, rank)
+    return select_clusters(keys, r)
+
+
 def reuse_groups(q: np.ndarray, q_prev: np.ndarray, group: int, tau: float) -> np.ndarray:
     """Speculative reuse with fine-grained correction (FreeKV technical
     summary §2.A.1-2): the retrieval set of the previous decoding step is
@@ -395,7 +423,8 @@ def decode(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np.ndar
            sink: int, window: int, r: int, scale: Optional[float] = None,
            heads: Optional[List[tuple]] = None, rank: str = "score",
            prev_q: Optional[np.ndarray] = None, prev_selected: Optional[dict] = None,
-           tau: float = 1.0) -> Dict[str, np.ndarray]:
+           tau: float = 1.0, share: str = "head",
+           index_dtype: str = "f32") -> Dict[str, np.ndarray]:
     """Decode attention for q [B, Hq, d] against K, V [B, Hkv, N, d] and a
     per-(b, kv head) index with leading [B, Hkv] axes.  Query head h reads KV
     head h // (Hq / Hkv) (grouped-query attention).  ``heads`` restricts the
@@ -405,7 +434,15 @@ def decode(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np.ndar
     With ``prev_q`` [B, Hq, d] and ``prev_selected`` ({(b, h): ids}) the
     previous step's selection is reused by every KV head that
     ``reuse_groups`` keeps at threshold ``tau``; the others select afresh.
-    ``reused`` [B, Hkv] reports the decision."""
+    ``reused`` [B, Hkv] reports the decision.
+
+    ``share="group"`` gives every query head of a KV head the group's shared
+    set (``group_selection``) instead of its own; ``index_dtype="bf16"``
+    decodes against ``round_index_bf16(index)``."""
+    if share not in ("head", "group") or index_dtype not in ("f32", "bf16"):
+        raise ValueError((share, index_dtype))
+    if index_dtype == "bf16":
+        index = round_index_bf16(index)
     B, Hq, d = q.shape
     Hkv = K.shape[1]
     group = Hq // Hkv
@@ -423,6 +460,9 @@ def decode(q: np.ndarray, K: np.ndarray, V: np.ndarray, index: Dict[str, np.ndar
         ih = {key: index[key][b, g] for key in ("size", "centroid_key", "value_sum", "perm",
                                                  "offset")}
         given = prev_selected[(b, h)] if reused[b, g] else None
+        if given is None and share == "group":
+            given = group_selection(q[b, g * group:(g + 1) * group], ih["centroid_key"],
+                                    ih["size"], scale, r, rank)
         res = decode_head(q[b, h], K[b, g], V[b, g], ih, sink, window, r, scale,
                           selected=given, rank=rank)
         out[b, h] = res["out"]

@@ -27,6 +27,10 @@ CASES = {
                              iters=3),
     "k100_short_tail": dict(B=1, Hkv=1, N=9000, sink=4, window=16, seg_len=2048, k=100, iters=2),
     "segment_below_k": dict(B=1, Hkv=1, N=1200, sink=4, window=16, seg_len=512, k=300, iters=2),
+    # the shipped index shape (8192-position segments, 512 clusters each): two
+    # full segments and a 4-position third one
+    "shipped_k512_seg8192": dict(B=1, Hkv=1, N=16900, sink=4, window=512, seg_len=8192, k=512,
+                                 iters=3),
 }
 
 
@@ -186,3 +190,27 @@ def test_bad_assignment_reports_status_not_fault():
     ix.assign_step(K)
     ix.update_step(K)
     assert ix.status() == 0
+
+
+def test_full_size_build_segment_agreement():
+    # The 128K-context index (8 KV heads, 16 segments of 512 clusters, 10
+    # iterations) built on the GPU in one call; one segment of one head is
+    # re-clustered by the oracle from the same strided start for the same 10
+    # iterations, and the final assignments must agree on >= 99.9% of its
+    # positions (rounding differences may cascade across iterations).
+    import cluster_indexed_sparse_wi_b300 as wl
+    w = WORKLOADS["llama3_8b_128k_b1"]
+    g = generate(w, want_q=False)
+    K, V = bf16_tensor(g["K"], "cuda"), bf16_tensor(g["V"], "cuda")
+    cfg = wl.IndexConfig(w.B, w.Hkv, w.N, w.sink, w.window, w.seg_len, w.k_per_seg, w.iters)
+    ix = wl.WaveIndex(cfg, "cuda").build(K, V)
+    torch.cuda.synchronize()
+    assert ix.status() == 0
+    h, s = 5, 9
+    pos = seg_positions(cfg)[s]
+    Kf = f64(g["K"][0, h][pos])
+    a_ref, _ = wi.kmeans_segment(Kf, w.k_per_seg, w.iters)
+    a_gpu = dl(ix.assign)[0, h][pos] - s * w.k_per_seg
+    agree = float(np.mean(a_gpu == a_ref))
+    print("128K segment assignment agreement", agree)
+    assert agree >= 0.999

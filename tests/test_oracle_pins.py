@@ -524,3 +524,85 @@ def test_reuse_per_group_decision():
     for b in range(B):
         for h in range(4):
             assert res["selected"][(b, h)].tolist() == [0, 1, 2]
+
+
+# ---------------------------------------------------------------- shared selection, bf16 index
+
+def test_round_index_bf16_matches_torch_cast_of_the_f32_index():
+    # torch's float32 -> bfloat16 cast (round to nearest even) of the stored
+    # float32 index; other arrays untouched
+    K, V, q, idx = small_case(seed=46, d=64)
+    r = wi.round_index_bf16(idx)
+    for key in ("centroid_key", "value_sum"):
+        ref = torch.from_numpy(idx[key].astype(np.float32)).to(torch.bfloat16).double().numpy()
+        np.testing.assert_array_equal(r[key], ref)
+    for key in ("size", "offset", "perm"):
+        assert r[key] is idx[key]
+
+
+def test_bf16_index_is_exact_for_bf16_representable_statistics():
+    # singleton clusters of bf16 keys and values: every mean key and value
+    # sum is already a bf16 value, so the bf16 index decodes identically
+    rng = np.random.default_rng(47)
+    B, Hkv, Hq, N, d = 1, 2, 4, 300, 32
+    K = bf16_vals(rng, (B, Hkv, N, d))
+    V = bf16_vals(rng, (B, Hkv, N, d))
+    q = bf16_vals(rng, (B, Hq, d))
+    idx = wi.build_index(K, V, 2, 10, 1024, N, 1)  # k >= tokens: the init makes singletons
+    assert idx["size"].max() == 1
+    a = wi.decode(q, K, V, idx, 2, 10, 7, 0.2)
+    b = wi.decode(q, K, V, idx, 2, 10, 7, 0.2, index_dtype="bf16")
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+
+
+def test_group_selection_bruteforce_sums():
+    # the shared set is the top r of sum_h s_h(c) computed by explicit loops
+    rng = np.random.default_rng(48)
+    for trial in range(20):
+        G, C, d = int(rng.integers(1, 5)), int(rng.integers(1, 40)), 8
+        kbar = rng.standard_normal((C, d))
+        n = rng.integers(0, 4, C)
+        qg = rng.standard_normal((G, d))
+        r = int(rng.integers(0, C + 2))
+        tot = []
+        for c in range(C):
+            if n[c] == 0:
+                continue
+            tot.append((-sum(0.3 * float(np.dot(qg[h], kbar[c])) for h in range(G)), c))
+        want = sorted(c for _, c in sorted(tot)[:r])
+        assert wi.group_selection(qg, kbar, n, 0.3, r).tolist() == want, trial
+        # with mass ranking each head adds ln n_c
+        tot = [(-sum(0.3 * float(np.dot(qg[h], kbar[c])) + math.log(n[c]) for h in range(G)), c)
+               for c in range(C) if n[c] > 0]
+        want = sorted(c for _, c in sorted(tot)[:r])
+        assert wi.group_selection(qg, kbar, n, 0.3, r, "mass").tolist() == want, trial
+
+
+def test_shared_decode_reduces_and_extends_per_head_decode():
+    # one query head per KV head: shared == per head, bit for bit; full budget:
+    # exact attention whatever the sharing; shared sets are common to a group
+    # and equal the set of the group's summed query
+    K, V, q, idx, z = _gqa_case(seed=49)
+    one = wi.decode(q[:, ::4], K, V, idx, z["sink"], z["window"], 5, 0.2)
+    one_s = wi.decode(q[:, ::4], K, V, idx, z["sink"], z["window"], 5, 0.2, share="group")
+    np.testing.assert_array_equal(one["out"], one_s["out"])
+    C = idx["n_clusters"]
+    full = wi.decode(q, K, V, idx, z["sink"], z["window"], C, 0.2, share="group")
+    ref = wi.decode(q, K, V, idx, z["sink"], z["window"], C, 0.2)
+    np.testing.assert_allclose(full["out"], ref["out"], rtol=1e-11, atol=1e-13)
+    res = wi.decode(q, K, V, idx, z["sink"], z["window"], 5, 0.2, share="group")
+    per = wi.decode(q, K, V, idx, z["sink"], z["window"], 5, 0.2)
+    B, Hq, _ = q.shape
+    differs = 0
+    for b in range(B):
+        for g in range(2):
+            sets = [res["selected"][(b, h)].tolist() for h in range(4 * g, 4 * g + 4)]
+            assert all(s == sets[0] for s in sets)
+            s_sum = wi.cluster_scores(q[b, 4 * g:4 * g + 4].sum(axis=0), idx["centroid_key"][b, g],
+                                      idx["size"][b, g], 0.2)
+            assert sets[0] == wi.select_clusters(s_sum, 5).tolist()
+            differs += sum(per["selected"][(b, h)].tolist() != sets[0] for h in range(4 * g, 4 * g + 4))
+    assert differs > 0
+    with pytest.raises(ValueError):
+        wi.decode(q, K, V, idx, z["sink"], z["window"], 5, 0.2, share="pair")
