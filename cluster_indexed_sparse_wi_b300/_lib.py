@@ -32,7 +32,8 @@ FIELDS = ["centroid_key", "unit_centroid", "value_sum", "size", "offset", "perm"
 SYMBOLS = [
     "wi_index_sizes", "wi_build_workspace_bytes", "wi_build_index", "wi_build_init",
     "wi_kmeans_assign", "wi_kmeans_update", "wi_build_finalize", "wi_decode_workspace_bytes",
-    "wi_decode_workspace_layout", "wi_decode_attention", "wi_decode_attention_ex",
+    "wi_decode_workspace_layout", "wi_decode_attention", "wi_index_round_bf16",
+    "wi_decode_attention_ex",
     "wi_decode_score", "wi_decode_select", "wi_decode_attend", "wi_decode_attention_static",
     "wi_decode_static_status", "wi_sync_status", "wi_status_string", "wi_debug_inject",
     "wi_version",
@@ -41,11 +42,16 @@ SYMBOLS = [
 WI_RANK_SCORE = 0
 WI_RANK_MASS = 1
 RANKS = {"score": WI_RANK_SCORE, "mass": WI_RANK_MASS}
+WI_SHARE_HEAD = 0
+WI_SHARE_GROUP = 1
+SHARES = {"head": WI_SHARE_HEAD, "group": WI_SHARE_GROUP}
 
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("rank", ctypes.c_int), ("tau", ctypes.c_float), ("prev_q", ctypes.c_void_p),
-                ("prev_topk", ctypes.c_void_p), ("reused", ctypes.c_void_p)]
+                ("prev_topk", ctypes.c_void_p), ("reused", ctypes.c_void_p),
+                ("share", ctypes.c_int), ("centroid_key_bf16", ctypes.c_void_p),
+                ("value_sum_bf16", ctypes.c_void_p)]
 
 
 class BuildParams(ctypes.Structure):
@@ -76,7 +82,8 @@ class IndexStruct(ctypes.Structure):
 class DecodeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("counters", "scores", "head_max", "selected", "sel_rows", "sel_counts",
-                 "sel_prefix", "sel_scores", "head_tokens", "partials", "total")] + [
+                 "sel_prefix", "sel_scores", "head_tokens", "group_values", "partials",
+                 "total")] + [
         (n, ctypes.c_int) for n in ("counter_bytes", "max_blocks", "reserved0", "reserved1")]
 
 
@@ -107,6 +114,7 @@ def lib() -> ctypes.CDLL:
         "wi_decode_workspace_bytes": (sz, [dp, i]),
         "wi_decode_workspace_layout": (i, [dp, i, P(DecodeLayout)]),
         "wi_decode_attention": (i, [dp, vp, vp, vp, ip, vp, vp, vp, vp, sz, vp]),
+        "wi_index_round_bf16": (i, [ip, vp, vp, vp]),
         "wi_decode_attention_ex": (i, [dp, P(DecodeOptions), vp, vp, vp, ip, vp, vp, vp, vp,
                                        sz, vp]),
         "wi_decode_score": (i, [dp, vp, ip, vp, sz, vp]),

@@ -173,6 +173,17 @@ class WaveIndex:
     def status(self, stream=None) -> int:
         return sync_status(self.workspace, stream)
 
+    def round_bf16(self, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+        """bf16 copies (round to nearest even) of the mean keys and value
+        sums: the leaner index a Decoder with index_dtype="bf16" streams."""
+        c = self.cfg
+        shape = (c.B, c.Hkv, c.n_clusters, c.d)
+        ck = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        vs = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        L.check(L.lib().wi_index_round_bf16(ctypes.byref(self.struct), _ptr(ck), _ptr(vs),
+                                            _stream(stream)), "wi_index_round_bf16")
+        return ck, vs
+
 
 def build_index(K: torch.Tensor, V: torch.Tensor, sink: int, window: int, seg_len: int,
                 k_per_seg: int, iters: int, stream=None) -> WaveIndex:
@@ -195,16 +206,27 @@ class Decoder:
     its workspace and output buffers.
 
     rank: "score" (the r largest cluster scores) or "mass" (the r largest
-    estimated attention masses n_c e^{s_c}).  A call given prev_q and
+    estimated attention masses n_c e^{s_c}).  share: "head" (every query head
+    selects its own set) or "group" (one set per KV group, on the group's
+    summed ranking keys).  index_dtype: "f32" streams the index's float32
+    mean keys and value sums; "bf16" streams bf16 copies of them (made once,
+    here, by WaveIndex.round_bf16), half the index bytes.  A call given prev_q and
     prev_topk (the previous step's queries and returned ids; prev_topk may be
     this decoder's own topk buffer) reuses the previous sets of every KV group
     whose queries all keep a cosine >= tau with their previous query."""
 
     def __init__(self, index: WaveIndex, Hq: int, r: int, scale: Optional[float] = None,
-                 rank: str = "score"):
+                 rank: str = "score", share: str = "head", index_dtype: str = "f32"):
         c = index.cfg
         if rank not in L.RANKS:
             raise ValueError("rank must be one of %s" % sorted(L.RANKS))
+        if share not in L.SHARES:
+            raise ValueError("share must be one of %s" % sorted(L.SHARES))
+        self.share = share
+        if index_dtype not in ("f32", "bf16"):
+            raise ValueError("index_dtype must be 'f32' or 'bf16'")
+        self.index_dtype = index_dtype
+        self.index16 = index.round_bf16() if index_dtype == "bf16" else None
         self.index = index
         self.Hq = Hq
         self.r = r
@@ -236,7 +258,8 @@ class Decoder:
         self._q(q)
         self.index._kv(K, V)
         topk = self.topk if (with_topk and self.r > 0) else None
-        if self.rank == "score" and prev_q is None:
+        if (self.rank == "score" and self.share == "head" and self.index16 is None
+                and prev_q is None):
             L.check(L.lib().wi_decode_attention(
                 ctypes.byref(self.params), _ptr(q), _ptr(K), _ptr(V),
                 ctypes.byref(self.index.struct), _ptr(self.out), _ptr(self.lse), _ptr(topk),
@@ -244,7 +267,11 @@ class Decoder:
                 "wi_decode_attention")
         else:
             c = self.index.cfg
-            opt = L.DecodeOptions(L.RANKS[self.rank], float(tau), None, None, _ptr(self.reused))
+            opt = L.DecodeOptions(L.RANKS[self.rank], float(tau), None, None, _ptr(self.reused),
+                                  L.SHARES[self.share])
+            if self.index16 is not None:
+                opt.centroid_key_bf16, opt.value_sum_bf16 = (_ptr(self.index16[0]),
+                                                             _ptr(self.index16[1]))
             if prev_q is not None:
                 _need(prev_q, "prev_q", torch.bfloat16, (c.B, self.Hq, c.d), self.index.device)
                 if prev_topk is None:

@@ -221,6 +221,8 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   off += align256(heads * rs * 4);
   L->head_tokens = off;
   off += align256(heads * 4);
+  L->group_values = off;
+  off += align256(groups * (size_t)C * 4);
   L->partials = off;
   off += align256(est_slots(p, C) * G * part);         // estimate pieces
   off += align256(groups * tph * G * part);            // steady pieces
@@ -267,7 +269,7 @@ namespace {
 
 int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, const void* V,
                      const wi_index* ix, void* ws, size_t ws_bytes, DecodeArgs* a,
-                     bool need_q, bool need_kv) {
+                     bool need_q, bool need_kv, const wi_decode_options* opt) {
   if (p == nullptr || ix == nullptr || ws == nullptr) return WI_ERR_INVALID_ARG;
   wi_decode_layout L;
   int st = decode_layout(p, ix->n_clusters, &L);
@@ -319,6 +321,10 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->V = static_cast<const uint16_t*>(V);
   a->kbar = ix->centroid_key;
   a->vsum = ix->value_sum;
+  if (opt != nullptr && opt->centroid_key_bf16 != nullptr) {
+    a->kbar16 = static_cast<const uint16_t*>(opt->centroid_key_bf16);
+    a->vsum16 = static_cast<const uint16_t*>(opt->value_sum_bf16);
+  }
   a->size = ix->size;
   a->offset = ix->offset;
   a->ksorted = static_cast<const uint16_t*>(ix->k_sorted);
@@ -341,6 +347,7 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   a->sel_pre = reinterpret_cast<int*>(w + L.sel_prefix);
   a->sel_sc = reinterpret_cast<float*>(w + L.sel_scores);
   a->head_tok = reinterpret_cast<int*>(w + L.head_tokens);
+  a->grp_vals = reinterpret_cast<float*>(w + L.group_values);
   const size_t part = (size_t)wi::kPartStride * 4;
   const DecodeShape d = decode_shape(p, C, nb);
   size_t off = L.partials;
@@ -365,7 +372,9 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   // and value sums, 64 KB per tile), steady tiles (32 KB) and selections
   const unsigned su = selection_units(C);
   for (int b = 0; b < nb; ++b) a->static_w[b] = 0u;
-  for (int j = 0; j < a->nchunks; ++j) a->static_w[j % nb] += 16u * (unsigned)wi::chunk_tiles(*a, j);
+  const unsigned tile_units = a->kbar16 ? 8u : 16u;  // both passes of one index tile
+  for (int j = 0; j < a->nchunks; ++j)
+    a->static_w[j % nb] += tile_units * (unsigned)wi::chunk_tiles(*a, j);
   const int nst = (int)groups * d.tph;
   for (int t = 0; t < nst; ++t) a->static_w[wi::steady_block(*a, t)] += 8u;
   for (size_t bh = 0; bh < heads; ++bh) a->static_w[wi::sel_block(*a, (int)bh)] += su;
@@ -373,8 +382,9 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
   // key tiles of every round (and, round by round, the value-sum tiles of
   // the earlier rounds) and one selection.  Work a block finishes before
   // then does not delay its retrieval share, so only the rest counts.
-  const unsigned wait =
-      8u * (unsigned)d.Q * (a->kbar_first ? (unsigned)d.rounds : 2u * (unsigned)d.rounds - 1u) + su;
+  const unsigned wait = tile_units / 2u * (unsigned)d.Q *
+                           (a->kbar_first ? (unsigned)d.rounds : 2u * (unsigned)d.rounds - 1u) +
+                       su;
   for (int b = 0; b < nb; ++b) a->static_w[b] = a->static_w[b] > wait ? a->static_w[b] - wait : 0u;
   a->static_units = 0;
   for (int b = 0; b < nb; ++b) a->static_units += a->static_w[b];
@@ -385,11 +395,14 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
 int check_options(const wi_decode_options* o, const wi_decode_params* p) {
   if (o == nullptr) return WI_OK;
   if (o->rank != WI_RANK_SCORE && o->rank != WI_RANK_MASS) return WI_ERR_INVALID_ARG;
+  if (o->share != WI_SHARE_HEAD && o->share != WI_SHARE_GROUP) return WI_ERR_INVALID_ARG;
   if (o->prev_q != nullptr && p != nullptr && p->r > 0) {
     if (o->prev_topk == nullptr || !(o->tau == o->tau)) return WI_ERR_INVALID_ARG;
     if (!aligned(o->prev_q, 16) || !aligned(o->prev_topk, 4)) return WI_ERR_ALIGNMENT;
   }
   if (!aligned(o->reused, 4)) return WI_ERR_ALIGNMENT;
+  if ((o->centroid_key_bf16 == nullptr) != (o->value_sum_bf16 == nullptr)) return WI_ERR_INVALID_ARG;
+  if (!aligned(o->centroid_key_bf16, 16) || !aligned(o->value_sum_bf16, 16)) return WI_ERR_ALIGNMENT;
   return WI_OK;
 }
 
@@ -401,10 +414,13 @@ int run_decode(const wi_decode_params* p, const void* q, const void* K, const vo
   DecodeArgs a;
   int st = check_options(opt, p);
   if (st != WI_OK) return st;
-  st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_q, need_kv);
+  st = fill_decode_args(p, q, K, V, index, workspace, workspace_bytes, &a, need_q, need_kv, opt);
   if (st != WI_OK) return st;
   if (opt != nullptr) {
     a.rank_mass = opt->rank == WI_RANK_MASS ? 1 : 0;
+    // (the static work estimates keep one selection per head: a group's
+    // selection costs about as much as its heads' would have together)
+    a.share = opt->share == WI_SHARE_GROUP ? 1 : 0;
     if (opt->prev_q != nullptr && p->r > 0) {
       a.prev_q = static_cast<const uint16_t*>(opt->prev_q);
       a.prev_topk = opt->prev_topk;
@@ -554,6 +570,26 @@ int wi_decode_attention(const wi_decode_params* p, const void* q, const void* K,
                         void* workspace, size_t workspace_bytes, wi_stream_t stream) {
   return run_decode(p, q, K, V, index, out, lse, topk_ids, workspace, workspace_bytes, stream,
                     wi::kStageScore | wi::kStageSelect | wi::kStageAttend, true, true);
+}
+
+int wi_index_round_bf16(const wi_index* index, void* centroid_key_bf16, void* value_sum_bf16,
+                        wi_stream_t stream) {
+  if (index == nullptr || centroid_key_bf16 == nullptr || value_sum_bf16 == nullptr ||
+      index->centroid_key == nullptr || index->value_sum == nullptr)
+    return WI_ERR_INVALID_ARG;
+  if (index->B <= 0 || index->Hkv <= 0 || index->n_clusters <= 0 || index->d != WI_HEAD_DIM)
+    return WI_ERR_INVALID_ARG;
+  if (!aligned(centroid_key_bf16, 16) || !aligned(value_sum_bf16, 16) ||
+      !aligned(index->centroid_key, 16) || !aligned(index->value_sum, 16))
+    return WI_ERR_ALIGNMENT;
+  int st = device_ok();
+  if (st != WI_OK) return st;
+  const size_t n = (size_t)index->B * index->Hkv * index->n_clusters * WI_HEAD_DIM;
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = wi::launch_round_bf16(index->centroid_key, static_cast<uint16_t*>(centroid_key_bf16), n, s);
+  if (e == cudaSuccess)
+    e = wi::launch_round_bf16(index->value_sum, static_cast<uint16_t*>(value_sum_bf16), n, s);
+  return cuda_status(e);
 }
 
 int wi_decode_attention_ex(const wi_decode_params* p, const wi_decode_options* options,

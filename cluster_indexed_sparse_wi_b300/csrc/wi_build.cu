@@ -13,6 +13,8 @@
 //   centroid_update_kernel: mu_j = bf16(normalize(sum k_i / ||k_i||)) over the
 //                           sorted members, f32, in position order.
 //   finalize_kernel       : mean key, value sum, cluster-sorted K/V copies.
+//   round_bf16_kernel     : bf16 copies of the mean keys and value sums (the
+//                           leaner index decode may stream instead).
 #include "wi_device.cuh"
 #include "wi_internal.h"
 
@@ -274,6 +276,28 @@ cudaError_t launch_cluster_sort(const BuildArgs& a, cudaStream_t st) {
 cudaError_t launch_centroid_update(const BuildArgs& a, cudaStream_t st) {
   const int bph = (a.C + kClustersPerBlock - 1) / kClustersPerBlock;
   cluster_reduce_kernel<false><<<a.B * a.Hkv * bph, kClusterThreads, 0, st>>>(a, bph);
+  return cudaGetLastError();
+}
+
+// dst[i] = bf16(src[i]) (round to nearest even), 4 values per thread step
+__global__ void round_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                  size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = src[i];
+    dst[i] = make_uint2((uint32_t)f2bf(v.x) | ((uint32_t)f2bf(v.y) << 16),
+                        (uint32_t)f2bf(v.z) | ((uint32_t)f2bf(v.w) << 16));
+  }
+}
+
+cudaError_t launch_round_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const size_t n4 = n / 4;  // n is a multiple of 128
+  round_bf16_kernel<<<sms * 4, 256, 0, st>>>(reinterpret_cast<const float4*>(src),
+                                             reinterpret_cast<uint2*>(dst), n4);
   return cudaGetLastError();
 }
 

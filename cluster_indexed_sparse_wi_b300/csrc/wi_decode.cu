@@ -80,6 +80,13 @@ static_assert(kSlots >= kStages + 1, "a warp may run kStages tiles ahead of the 
 
 enum : int { kTileRet = 1, kTileEnd = 2 };
 
+// With a bf16 index a stage carries tiles i and i + 1 of chunk j (n tiles)
+// when both exist and belong to one KV group; producer and consumers pair
+// tiles by this rule.
+__device__ __forceinline__ bool pair_tiles(const DecodeArgs& a, int j, int i, int n) {
+  return a.kbar16 != nullptr && i + 1 < n && (j * a.Q + i + 1) % a.tpg != 0;
+}
+
 // Retrieval tile description, written by the producer with the tile.
 struct TileInfo {
   int kind;
@@ -110,8 +117,8 @@ struct __align__(128) DecSmem {
   unsigned char ring[kStages][kStageBytes];  // bulk-copy destinations
   unsigned char qs[kStages][kQSlotBytes];    // query rows staged with a tile
   union __align__(16) {
-    int n[kTile];    // index tiles: cluster sizes
-    float s[kTile];  // retrieval tiles: the cluster score of each token (log2 units)
+    int n[2 * kTile];  // index tiles: cluster sizes (two tiles per stage with a bf16 index)
+    float s[kTile];    // retrieval tiles: the cluster score of each token (log2 units)
   } side[kStages];
   union __align__(16) {
     struct {
@@ -390,18 +397,15 @@ __device__ void combine_write(DecSmem& S, const float (&m)[NH], const float (&l)
 // Returns the number selected, or -1 (nothing written) when b* holds more
 // than kCand values or the ids do not fit the bitmap: the general path then
 // takes over.
-__device__ int select_fast(const DecodeArgs& a, DecSmem& S, int bh, int* ids, int* topk) {
+__device__ int select_fast(const DecodeArgs& a, DecSmem& S, const float* sc, const int* sz,
+                           bool mass, float* hm_out, int* ids, int* topk) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bg = bh / a.G;
   const int C = a.C, r = a.r;
-  const float* sc = a.scores + (size_t)bh * C;
-  const int* sz = a.size + (size_t)bg * C;
   const int nch = (C + kSelChunk - 1) / kSelChunk;
   const int nwords = (C + 31) / 32;
   if (nwords > 16 * kCT) return -1;  // the bitmap lives in S.u.sel.key
   uint32_t* bits = &S.u.sel.key[0][0];
   const bool vec = (C & 3) == 0;
-  const bool mass = a.rank_mass != 0;
   float smx = -INFINITY;  // largest score (differs from the largest v when ranking by mass)
   auto mval = [](float s, int n) { return n > 0 ? s + logf((float)n) : -INFINITY; };
   // values of chunk ch for this thread
@@ -520,7 +524,7 @@ __device__ int select_fast(const DecodeArgs& a, DecSmem& S, int bh, int* ids, in
     }
   }
   const int r_eff = min(r, cnt);
-  if (tid == 0) a.head_max[bh] = cnt > 0 ? smx : -INFINITY;
+  if (tid == 0 && hm_out) *hm_out = cnt > 0 ? smx : -INFINITY;
   if (r_eff == 0) return 0;
 
   // B. histogram and boundary bin (skipped when every valid id is taken)
@@ -654,12 +658,17 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bg = bh / a.G;
   const int C = a.C, r = a.r, rs = r > 0 ? r : 1;
-  const float* sc = a.scores + (size_t)bh * C;
+  // shared selection: bh is the group's first head and the set is chosen on
+  // the group's summed ranking keys (written to a.grp_vals below), then
+  // recorded for every head of the group
+  const bool shared = a.share != 0;
+  const int nh = shared ? a.G : 1;
+  const float* sc = shared ? a.grp_vals + (size_t)bg * C : a.scores + (size_t)bh * C;
   const int* sz = a.size + (size_t)bg * C;
   const int* off = a.offset + (size_t)bg * (C + 1);
   const int nch = (C + kSelChunk - 1) / kSelChunk;
   const bool vec = (C & 3) == 0;  // rows of scores and sizes start on 16-byte boundaries
-  const bool mass = a.rank_mass != 0;
+  const bool mass = a.rank_mass != 0 && !shared;  // the group row holds the mass keys already
   int buf = 0;
 
   // ranking key of the mass order: s_c + ln n_c (0 for an empty cluster)
@@ -794,9 +803,46 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
       }
     }
   }
-  if (tid == 0 && a.reused != nullptr) a.reused[bh] = reuse ? 1 : 0;
-  int* topk = a.topk_out ? a.topk_out + (size_t)bh * r : nullptr;
-  const int n_fast = reuse ? -1 : select_fast(a, S, bh, ids, topk);
+  if (tid < nh && a.reused != nullptr) a.reused[bh + tid] = reuse ? 1 : 0;
+  if (shared) {
+    // the group row v_c = sum_h key_h(c) and every head's largest score
+    const float* s0 = a.scores + (size_t)bh * C;
+    float hm[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) hm[h] = -INFINITY;
+    for (int c = tid; c < C; c += kCT) {
+      const int n = __ldg(sz + c);
+      const float lg = (a.rank_mass && n > 0) ? logf((float)n) : 0.f;
+      float v = 0.f;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        if (h < nh) {
+          const float sv = __ldcg(s0 + (size_t)h * C + c);
+          hm[h] = fmaxf(hm[h], sv);
+          v += sv + lg;
+        }
+      }
+      a.grp_vals[(size_t)bg * C + c] = n > 0 ? v : -INFINITY;
+    }
+    float* red = reinterpret_cast<float*>(S.u.sel.hist);  // [8][kCW] partial maxima
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      float x = hm[h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+      if (lane == 0) red[h * kCW + warp] = x;
+    }
+    csync();
+    if (tid < nh) {
+      float x = -INFINITY;
+      for (int w = 0; w < kCW; ++w) x = fmaxf(x, red[tid * kCW + w]);
+      a.head_max[bh + tid] = x;
+    }
+    csync();  // the group row is written; the partial maxima are read
+  }
+  int* topk = (a.topk_out && !shared) ? a.topk_out + (size_t)bh * r : nullptr;
+  const int n_fast =
+      reuse ? -1 : select_fast(a, S, sc, sz, mass, shared ? nullptr : a.head_max + bh, ids, topk);
   const bool general = !reuse && n_fast < 0;
 
   // 1. keys of the first chunk into shared memory; count and key range; the
@@ -809,7 +855,7 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     kmax = max(kmax, k);
     kmin = min(kmin, k != 0u ? k : 0xffffffffu);
   };
-  if (reuse || (general && mass)) {
+  if (!shared && (reuse || (general && mass))) {
     for (int c = tid; c < C; c += kCT) smax = max(smax, score_key(__ldcg(sc + c)));
   }
   if (general) {
@@ -822,7 +868,7 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   }
   if (reuse || general) {
     block_count_range(valid, kmax, kmin, smax);
-    if (tid == 0) a.head_max[bh] = smax != 0u ? key_float(smax) : -INFINITY;
+    if (tid == 0 && !shared) a.head_max[bh] = smax != 0u ? key_float(smax) : -INFINITY;
   }
   const int r_eff = reuse ? n_reuse : (general ? min(r, valid) : n_fast);
 
@@ -974,10 +1020,6 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   }
 
   // 4. ids in ascending order, then each selected cluster's size, row, score
-  int* rows = a.sel_rows + rsel0;
-  int* cnts = a.sel_cnts + rsel0;
-  int* pre = a.sel_pre + rsel0;
-  float* ssel = a.sel_sc + rsel0;
   int sel_base = 0;
   if (r_eff > 0 && general) {
     for (int ch = 0; ch < nch; ++ch) {
@@ -1012,17 +1054,20 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
   }
   const int nsel_tot = general ? min(sel_base, r) : r_eff;  // == r_eff
   csync();  // the ids are written (and visible to the block)
+  // every head of the set (one, or the group's nh when shared): the same ids,
+  // rows, sizes and token offsets, and the head's own scores
+  const bool topk_here = a.topk_out != nullptr && (reuse || shared);
+  const float* s_own = a.scores + (size_t)bh * C;
   int tok_base = 0;
   for (int i0 = 0; i0 < nsel_tot; i0 += kCT) {
     const int i = i0 + tid;
-    int n = 0, row = 0;
+    int n = 0, row = 0, c = -1;
     float sv = -INFINITY;
     if (i < nsel_tot) {
-      const int c = ids[i];
-      if (reuse && topk) topk[i] = c;
+      c = ids[i];
       n = __ldg(sz + c);
       row = __ldg(off + c);
-      sv = __ldcg(sc + c);
+      sv = __ldcg(s_own + c);
       if (n < 0 || row < 0 || (long long)row + n > a.N_idx) {
         report(a.status, WI_ERR_INDEX_MISMATCH);  // inconsistent index: stage nothing
         n = 0;
@@ -1032,22 +1077,30 @@ __device__ int select_head(const DecodeArgs& a, DecSmem& S, int bh) {
     int2 tot;
     const int ex = cscan2(make_int2(n, 0), S, &tot, buf).x;
     if (i < nsel_tot) {
-      rows[i] = row;
-      cnts[i] = n;
-      pre[i] = tok_base + ex;
-      ssel[i] = sv;
+      for (int h = 0; h < nh; ++h) {
+        const size_t o = (size_t)(bh + h) * rs + i;
+        a.sel_ids[o] = c;
+        a.sel_rows[o] = row;
+        a.sel_cnts[o] = n;
+        a.sel_pre[o] = tok_base + ex;
+        a.sel_sc[o] = h == 0 ? sv : __ldcg(s_own + (size_t)h * C + c);
+        if (topk_here) a.topk_out[(size_t)(bh + h) * r + i] = c;
+      }
     }
     tok_base += tot.x;
   }
-  for (int i = nsel_tot + tid; i < rs; i += kCT) {
-    ids[i] = -1;
-    rows[i] = 0;
-    cnts[i] = 0;
-    pre[i] = tok_base;
-    ssel[i] = -INFINITY;
-    if (topk && i < r) topk[i] = -1;
+  for (int h = 0; h < nh; ++h) {
+    for (int i = nsel_tot + tid; i < rs; i += kCT) {
+      const size_t o = (size_t)(bh + h) * rs + i;
+      a.sel_ids[o] = -1;
+      a.sel_rows[o] = 0;
+      a.sel_cnts[o] = 0;
+      a.sel_pre[o] = tok_base;
+      a.sel_sc[o] = -INFINITY;
+      if (a.topk_out && i < r) a.topk_out[(size_t)(bh + h) * r + i] = -1;
+    }
   }
-  if (tid == 0) a.head_tok[bh] = tok_base;
+  if (tid < nh) a.head_tok[bh + tid] = tok_base;
   csync();  // the selection is complete after this barrier
   return nsel_tot;
 }
@@ -1255,18 +1308,24 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
           const int j = rd * a.nb + (int)blockIdx.x;
           if (j >= a.nchunks) continue;
           const int n = chunk_tiles(a, j);
-          const float* src = pass == 0 ? a.kbar : a.vsum;
+          // f32 rows (512 B), or bf16 rows (256 B) with two tiles of one group per stage
+          const bool h16 = a.kbar16 != nullptr;
+          const unsigned char* src =
+              h16 ? reinterpret_cast<const unsigned char*>(pass == 0 ? a.kbar16 : a.vsum16)
+                  : reinterpret_cast<const unsigned char*>(pass == 0 ? a.kbar : a.vsum);
+          const uint32_t rowb = h16 ? 256u : 512u;
           int bg = (j * a.Q) / a.tpg, c0 = (j * a.Q - bg * a.tpg) * kTile;
           int q_bg = -1;  // the group whose query rows were staged last
-          for (int i = 0; i < n; ++i) {
-            const int nrows = min(kTile, a.C - c0);
+          for (int i = 0; i < n;) {
+            const int nsub = pair_tiles(a, j, i, n) ? 2 : 1;
+            const int nrows = min(nsub * kTile, a.C - c0);
             int stage;
             if (!wait_slot(stage)) {
               ok = false;
               break;
             }
             const size_t row0 = (size_t)bg * a.C + c0;
-            uint32_t bytes = (uint32_t)nrows * 512u;
+            uint32_t bytes = (uint32_t)nrows * rowb;
             const bool bulk_n = side_bulk && (nrows & 3) == 0;
             const bool with_q = pass == 0 && bg != q_bg;
             if (pass == 0) {
@@ -1274,11 +1333,12 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
               if (bulk_n) {
                 bytes += (uint32_t)nrows * 4u;
               } else {  // ragged rows of sizes: plain loads before the tile is posted
-                for (int c = 0; c < kTile; ++c) S.side[stage].n[c] = c < nrows ? __ldg(a.size + row0 + c) : 0;
+                for (int c = 0; c < nsub * kTile; ++c)
+                  S.side[stage].n[c] = c < nrows ? __ldg(a.size + row0 + c) : 0;
               }
             }
             mbar_arrive_expect_tx(smem_addr(&S.full[stage]), bytes);
-            issue(S.ring[stage], src + row0 * kD, (uint32_t)nrows * 512u, stage);
+            issue(S.ring[stage], src + row0 * rowb, (uint32_t)nrows * rowb, stage);
             if (with_q) {  // the consumers read the query rows with a group's first tile
               const int b = bg / a.Hkv, g = bg - b * a.Hkv;
               issue(S.qs[stage], a.q + ((size_t)b * a.Hq + (size_t)g * G) * kD,
@@ -1288,7 +1348,8 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
             if (pass == 0 && bulk_n)
               issue(S.side[stage].n, a.size + row0, (uint32_t)nrows * 4u, stage);
             done_tile();
-            c0 += kTile;
+            i += nsub;
+            c0 += nsub * kTile;
             if (c0 >= a.C) {
               c0 = 0;
               ++bg;
@@ -1632,7 +1693,7 @@ __device__ bool wait_count_all(const DecodeArgs& a, DecSmem& S, const unsigned* 
 // Centroid-key tiles of chunk j (n tiles): scores of the group's G heads,
 // into the workspace and the block's chunk copy; then the groups' scored-tile
 // counts are published.
-template <int G>
+template <int G, bool H16>
 __device__ __forceinline__ void kbar_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L4 = 4 * G;
@@ -1645,53 +1706,64 @@ __device__ __forceinline__ void kbar_tiles(const DecodeArgs& a, DecSmem& S, Ring
   float* srow = nullptr;  // scores row of this lane's head
 #pragma unroll
   for (int h = 0; h < G; ++h) qs[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < n; ++i) {
-    const int nrows = min(kTile, C - c0);
+  for (int i = 0; i < n;) {
+    const int nsub = (H16 && pair_tiles(a, j, i, n)) ? 2 : 1;
     int stage;
-    if (acquire(a, S, rg, stage)) {
-      float4 k[4];
-      const float* kb = reinterpret_cast<const float*>(S.ring[stage]);
-#pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) {
-        const int row = warp * 4 + r4;
-        k[r4] = row < nrows ? lds4(kb + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      if (bg != cur_bg) {  // the group's query rows come with its first tile
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 qf = bf4(lds2(S.qs[stage] + h * kD * 2 + lane * 8));
-          qs[h] = make_float4(qf.x * a.scale, qf.y * a.scale, qf.z * a.scale, qf.w * a.scale);
-        }
-        cur_bg = bg;
-        const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-        srow = a.scores + ((size_t)b * a.Hq + (size_t)g * G + hr) * C;
-      }
-      const int nsz = S.side[stage].n[warp * 4 + jr];
-      release(S, rg, stage);
-      float v[4 * G];
+    const bool got = acquire(a, S, rg, stage);
+    if (got && bg != cur_bg) {  // the group's query rows come with its first tile
 #pragma unroll
       for (int h = 0; h < G; ++h) {
+        const float4 qf = bf4(lds2(S.qs[stage] + h * kD * 2 + lane * 8));
+        qs[h] = make_float4(qf.x * a.scale, qf.y * a.scale, qf.z * a.scale, qf.w * a.scale);
+      }
+      cur_bg = bg;
+      const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+      srow = a.scores + ((size_t)b * a.Hq + (size_t)g * G + hr) * C;
+    }
+    for (int sub = 0; sub < nsub; ++sub) {  // the tiles of the stage (one group)
+      const int nrows = min(kTile, C - c0);
+      const int ii = i + sub;
+      if (got) {
+        float4 k[4];
 #pragma unroll
-        for (int r4 = 0; r4 < 4; ++r4)
-          v[r4 * G + h] = k[r4].x * qs[h].x + k[r4].y * qs[h].y + k[r4].z * qs[h].z + k[r4].w * qs[h].w;
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const int row = warp * 4 + r4;
+          if (H16) {
+            const uint16_t* kb = reinterpret_cast<const uint16_t*>(S.ring[stage]) + sub * kTile * kD;
+            k[r4] = row < nrows ? bf4(lds2(kb + row * kD + lane * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            const float* kb = reinterpret_cast<const float*>(S.ring[stage]);
+            k[r4] = row < nrows ? lds4(kb + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        const int nsz = S.side[stage].n[sub * kTile + warp * 4 + jr];
+        if (sub == nsub - 1) release(S, rg, stage);
+        float v[4 * G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+          for (int r4 = 0; r4 < 4; ++r4)
+            v[r4 * G + h] = k[r4].x * qs[h].x + k[r4].y * qs[h].y + k[r4].z * qs[h].z + k[r4].w * qs[h].w;
+        }
+        const float tot = reduce_scatter<4 * G>(v, lane);
+        const int row = warp * 4 + jr;
+        const float s = (row < nrows && nsz > 0) ? tot : -INFINITY;
+        if (lane < L4) {
+          if (row < nrows) srow[c0 + row] = s;
+          S.a.chunk.sc[ii][warp][lane] = s;
+          if (hr == 0) S.a.chunk.n[ii][warp][jr] = row < nrows ? nsz : 0;
+        }
+      } else if (lane < L4) {
+        S.a.chunk.sc[ii][warp][lane] = -INFINITY;
+        if (hr == 0) S.a.chunk.n[ii][warp][jr] = 0;
       }
-      const float tot = reduce_scatter<4 * G>(v, lane);
-      const int row = warp * 4 + jr;
-      const float s = (row < nrows && nsz > 0) ? tot : -INFINITY;
-      if (lane < L4) {
-        if (row < nrows) srow[c0 + row] = s;
-        S.a.chunk.sc[i][warp][lane] = s;
-        if (hr == 0) S.a.chunk.n[i][warp][jr] = row < nrows ? nsz : 0;
+      c0 += kTile;
+      if (c0 >= C) {
+        c0 = 0;
+        ++bg;
       }
-    } else if (lane < L4) {
-      S.a.chunk.sc[i][warp][lane] = -INFINITY;
-      if (hr == 0) S.a.chunk.n[i][warp][jr] = 0;
     }
-    c0 += kTile;
-    if (c0 >= C) {
-      c0 = 0;
-      ++bg;
-    }
+    i += nsub;
   }
   if (n > 0) {
     csync();  // every warp's scores of the chunk are written
@@ -1739,12 +1811,12 @@ __device__ __forceinline__ void selections(const DecodeArgs& a, DecSmem& S, cons
       const int lc = last_chunk(a, bg);
       int hl = (lc - blk) % a.nb;
       if (hl < 0) hl += a.nb;
-      if (hl >= G) continue;
+      if (hl >= (a.share ? 1 : G)) continue;
       const int bh = bg * G + hl;
       const bool ok = a.fused ? wait_count_all(a, S, a.grp_cnt + bg, (unsigned)a.tpg) : !cany(rg.hollow);
       if (!ok) continue;
       select_head(a, S, bh);
-      if (a.fused && tid == 0) publish(S, a, a.sel_done, 1u, 1);
+      if (a.fused && tid == 0) publish(S, a, a.sel_done, a.share ? (unsigned)G : 1u, 1);
     }
   }
 }
@@ -1752,7 +1824,7 @@ __device__ __forceinline__ void selections(const DecodeArgs& a, DecSmem& S, cons
 // Value-sum tiles of chunk j: the estimate of every cluster of the chunk,
 // against the warp's own maximum score of each KV group (a fixed reference:
 // no rescaling), one partial per (chunk, KV group, query head).
-template <int G>
+template <int G, bool H16>
 __device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring& rg, int j, int n,
                                            bool refill) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1800,19 +1872,29 @@ __device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring
 #pragma unroll
     for (int h = 1; h < G; ++h)
       if (hr == h) mL = m[h];
-    for (int i = i0; i < i1; ++i) {
+    for (int i = i0; i < i1;) {
+      const int nsub = (H16 && pair_tiles(a, j, i, n)) ? 2 : 1;
+      int stage;
+      if (!acquire(a, S, rg, stage)) {
+        i += nsub;
+        continue;
+      }
+      for (int sub = 0; sub < nsub; ++sub, ++i) {  // the tiles of the stage (one group)
       const int c0 = (j * a.Q + i - bg * a.tpg) * kTile;
       const int nrows = min(kTile, a.C - c0);
-      int stage;
-      if (!acquire(a, S, rg, stage)) continue;
       float4 v[4];
-      const float* vs = reinterpret_cast<const float*>(S.ring[stage]);
 #pragma unroll
       for (int r4 = 0; r4 < 4; ++r4) {
         const int row = warp * 4 + r4;
-        v[r4] = row < nrows ? lds4(vs + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (H16) {
+          const uint16_t* vs = reinterpret_cast<const uint16_t*>(S.ring[stage]) + sub * kTile * kD;
+          v[r4] = row < nrows ? bf4(lds2(vs + row * kD + lane * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          const float* vs = reinterpret_cast<const float*>(S.ring[stage]);
+          v[r4] = row < nrows ? lds4(vs + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-      release(S, rg, stage);
+      if (sub == nsub - 1) release(S, rg, stage);
       const float s = lane < L4 ? S.a.chunk.sc[i][warp][lane] : -INFINITY;
       const int nn = lane < L4 ? S.a.chunk.n[i][warp][jr] : 0;
       const float p = (s > -INFINITY && nn > 0) ? exp2f(s * kLog2e - mL) : 0.f;
@@ -1827,6 +1909,7 @@ __device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring
           o[h].z += pj * v[jj].z;
           o[h].w += pj * v[jj].w;
         }
+      }
       }
     }
     // est partial slot of (chunk j, group bg): (j + bg) * G + h
@@ -2106,10 +2189,16 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S) {
     const int n = chunk_n(rd);
     if (n == 0) continue;
     if (kind == 0) {
-      kbar_tiles<G>(a, S, rg, rd * a.nb + blk, n);
+      if (a.kbar16)
+        kbar_tiles<G, true>(a, S, rg, rd * a.nb + blk, n);
+      else
+        kbar_tiles<G, false>(a, S, rg, rd * a.nb + blk, n);
       last_rd = rd;
     } else {
-      vsum_tiles<G>(a, S, rg, rd * a.nb + blk, n, a.kbar_first && rd != last_rd);
+      if (a.kbar16)
+        vsum_tiles<G, true>(a, S, rg, rd * a.nb + blk, n, a.kbar_first && rd != last_rd);
+      else
+        vsum_tiles<G, false>(a, S, rg, rd * a.nb + blk, n, a.kbar_first && rd != last_rd);
     }
   }
   if (a.stages & kStageAttend) {

@@ -60,6 +60,8 @@ struct DecodeArgs {
   const uint16_t* V;
   const float* kbar;        // f32 [B,Hkv,C,128]
   const float* vsum;        // f32 [B,Hkv,C,128]
+  const uint16_t* kbar16;   // bf16 copies of kbar / vsum [B,Hkv,C,128], or null (f32 index)
+  const uint16_t* vsum16;
   const int* size;          // [B,Hkv,C]
   const int* offset;        // [B,Hkv,C+1]
   const uint16_t* ksorted;  // bf16 [B,Hkv,N_idx,128]
@@ -81,6 +83,7 @@ struct DecodeArgs {
   int* sel_pre;         // [B,Hq,rs]  members of the clusters before it (token offset)
   float* sel_sc;        // [B,Hq,rs]  its score s_c
   int* head_tok;        // [B,Hq]     retrieved tokens of the head
+  float* grp_vals;      // [B,Hkv,C]  shared selection: summed ranking keys
   float* est_part;      // [(nchunks + B*Hkv) * G][kPartStride]
   float* std_part;      // [B*Hkv*tph * G][kPartStride]
   float* ret_part;      // [(nb + B*Hq)][kPartStride]
@@ -98,6 +101,7 @@ struct DecodeArgs {
   int inject;           // test hook: every block skips the copies of its first tile
   // selection options
   int rank_mass;        // rank clusters by s_c + ln n_c instead of s_c
+  int share;            // one retrieval set per KV group (summed ranking keys)
   float tau;            // reuse threshold on the group's smallest query cosine
   const uint16_t* prev_q;  // bf16 [B,Hq,128] previous step's queries, or null (no reuse)
   const int* prev_topk;    // [B,Hq,r] previous step's retrieved ids (ascending, -1 padding)
@@ -158,5 +162,7 @@ cudaError_t launch_kmeans_assign(const BuildArgs& a, cudaStream_t st);
 cudaError_t launch_cluster_sort(const BuildArgs& a, cudaStream_t st);
 cudaError_t launch_centroid_update(const BuildArgs& a, cudaStream_t st);
 cudaError_t launch_finalize_stats(const BuildArgs& a, cudaStream_t st);
+// dst[i] = bf16(src[i]) for i < n (n a multiple of 4; 16-byte aligned arrays)
+cudaError_t launch_round_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st);
 
 }  // namespace wi

@@ -201,6 +201,8 @@ typedef struct {
   size_t sel_prefix;    /* i32 [B,Hq,max(r,1)]  retrieved tokens before it       */
   size_t sel_scores;    /* f32 [B,Hq,max(r,1)]  its score s_c (-inf padding)     */
   size_t head_tokens;   /* i32 [B,Hq]     retrieved tokens of the head           */
+  size_t group_values;  /* f32 [B,Hkv,C]  shared selection: the group's summed
+                           ranking keys (-inf if empty)                      */
   size_t partials;      /* f32 partials: estimate pieces (per chunk of index
                            tiles and query head), steady pieces (per steady
                            tile and query head), retrieval pieces            */
@@ -240,6 +242,8 @@ WI_API int wi_decode_attention(const wi_decode_params *p, const void *q, const v
 
 /* Ranking keys of the retrieval zone (wi_decode_options.rank). */
 enum { WI_RANK_SCORE = 0, WI_RANK_MASS = 1 };
+/* Granularity of the retrieval zone (wi_decode_options.share). */
+enum { WI_SHARE_HEAD = 0, WI_SHARE_GROUP = 1 };
 
 /* Options of wi_decode_attention_ex.  All-zero options (rank WI_RANK_SCORE,
  * prev_q NULL, reused NULL) give wi_decode_attention. */
@@ -267,11 +271,33 @@ typedef struct {
   const int32_t *prev_topk;  /* i32 [B,Hq,r] device (required with prev_q)      */
   int32_t *reused;           /* i32 [B,Hq] device or NULL: 1 where the head took
                                 its previous set, else 0                         */
+  /* WI_SHARE_HEAD: every query head selects its own set.  WI_SHARE_GROUP:
+   * one set per KV group, the r largest summed ranking keys
+   * sum_h key_h(c) over the group's query heads (ties to the lower id);
+   * every head of the group attends over it with its own logits and scores
+   * (the selection granularity is left open by technical summary (es)
+   * §2.A.2).  With reuse, a group takes its first head's previous set. */
+  int share;
+  /* Leaner index: bf16 copies of index->centroid_key and index->value_sum
+   * (bf16 [B,Hkv,C,d] device, 16-byte aligned, as wi_index_round_bf16
+   * writes them), both or neither.  When set, decode streams these instead of
+   * the f32 arrays (half the index bytes); scores and estimates use the
+   * rounded values. */
+  const void *centroid_key_bf16;
+  const void *value_sum_bf16;
 } wi_decode_options;
 
+/* The bf16 copies of a built index's mean keys and value sums used by
+ * wi_decode_options.centroid_key_bf16 / value_sum_bf16: each element is the
+ * f32 value rounded to nearest even.  Output arrays bf16 [B,Hkv,C,d] (device,
+ * 16-byte aligned, caller-owned).  WI_ERR_INVALID_ARG for null pointers or an
+ * index without recorded shape. */
+WI_API int wi_index_round_bf16(const wi_index *index, void *centroid_key_bf16, void *value_sum_bf16,
+                        wi_stream_t stream);
+
 /* wi_decode_attention with selection options (options may be NULL).
- * Returns WI_ERR_INVALID_ARG for an unknown rank, prev_q without prev_topk
- * or a NaN tau, and WI_ERR_ALIGNMENT for misaligned option pointers, before
+ * Returns WI_ERR_INVALID_ARG for an unknown rank or share, prev_q without
+ * prev_topk, a NaN tau or only one of the bf16 index arrays, and WI_ERR_ALIGNMENT for misaligned option pointers, before
  * anything is enqueued. */
 WI_API int wi_decode_attention_ex(const wi_decode_params *p, const wi_decode_options *options,
                            const void *q, const void *K, const void *V,

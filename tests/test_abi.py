@@ -120,8 +120,8 @@ def test_decode_layout(L):
     assert lib.wi_decode_workspace_layout(ctypes.byref(dp(L)), 256, ctypes.byref(lay)) == 0
     assert lay.total == lib.wi_decode_workspace_bytes(ctypes.byref(dp(L)), 256)
     regions = [lay.counters, lay.scores, lay.head_max, lay.selected, lay.sel_rows,
-               lay.sel_counts, lay.sel_prefix, lay.sel_scores, lay.head_tokens, lay.partials,
-               lay.total]
+               lay.sel_counts, lay.sel_prefix, lay.sel_scores, lay.head_tokens,
+               lay.group_values, lay.partials, lay.total]
     assert regions == sorted(regions) and all(r % 256 == 0 for r in regions)
     assert lay.head_max - lay.scores >= 8 * 256 * 4
     # launch-wide words, then one scored-tile counter per KV group and one
@@ -131,6 +131,7 @@ def test_decode_layout(L):
                    (lay.sel_counts, lay.sel_prefix), (lay.sel_prefix, lay.sel_scores),
                    (lay.sel_scores, lay.head_tokens)):
         assert hi - lo >= 8 * 8 * 4
+    assert lay.partials - lay.group_values >= 2 * 256 * 4  # [B, Hkv, C] f32
     # partials, (m, l, o[128]) each: estimate pieces (at most one per index
     # tile and KV group, G heads each), steady pieces (2 tiles per KV group, G
     # heads each), retrieval pieces (one per block and query head)
@@ -191,6 +192,7 @@ def test_decode_option_validation(L):
                                           ctypes.byref(ix), fake, None, None, fake, 1 << 30, None)
 
     assert call(rank=2) == L.WI_ERR_INVALID_ARG
+    assert call(share=2) == L.WI_ERR_INVALID_ARG
     assert call(rank=-1) == L.WI_ERR_INVALID_ARG
     assert call(prev_q=1 << 20) == L.WI_ERR_INVALID_ARG              # no prev_topk
     assert call(prev_q=1 << 20, prev_topk=1 << 20, tau=float("nan")) == L.WI_ERR_INVALID_ARG

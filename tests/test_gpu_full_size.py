@@ -11,6 +11,7 @@ KV group).
   selection values re-read per pass.
 * 128K context, batch 16: seven rounds of index tiles (value-sum tiles of
   earlier rounds read their scores back), heads of several sequences.
+* 128K context with the bf16 index (two index tiles per staging stage).
 
 Tolerances are those of test_gpu_decode:
 * cluster scores: relative 1e-5;
@@ -42,11 +43,12 @@ def gpu_head_index(ix, b, g):
             "offset": ix.offset[b, g].cpu().numpy().astype(np.int64)}
 
 
-@pytest.mark.parametrize("name,heads", [
-    ("llama3_8b_128k_b1", [(0, 0), (0, 13), (0, 22), (0, 31)]),
-    ("llama3_8b_1m_b1", [(0, 5), (0, 30)]),
-    ("llama3_8b_128k_b16", [(0, 3), (7, 17), (15, 30)])])
-def test_full_size_sampled_heads(name, heads):
+@pytest.mark.parametrize("name,heads,index_dtype", [
+    ("llama3_8b_128k_b1", [(0, 0), (0, 13), (0, 22), (0, 31)], "f32"),
+    ("llama3_8b_128k_b1", [(0, 2), (0, 29)], "bf16"),
+    ("llama3_8b_1m_b1", [(0, 5), (0, 30)], "f32"),
+    ("llama3_8b_128k_b16", [(0, 3), (7, 17), (15, 30)], "f32")])
+def test_full_size_sampled_heads(name, heads, index_dtype):
     import cluster_indexed_sparse_wi_b300 as wl
     w = WORKLOADS[name]
     g = generate(w)
@@ -57,7 +59,7 @@ def test_full_size_sampled_heads(name, heads):
     ix.build(K, V)
     torch.cuda.synchronize()
     assert ix.status() == 0
-    dec = wl.Decoder(ix, w.Hq, w.r)
+    dec = wl.Decoder(ix, w.Hq, w.r, index_dtype=index_dtype)
     out, lse, topk = dec(q, K, V)
     torch.cuda.synchronize()
     assert dec.status() == 0
@@ -68,8 +70,11 @@ def test_full_size_sampled_heads(name, heads):
     for b, h in heads:
         gg = h // G
         if (b, gg) not in groups:
+            hi = gpu_head_index(ix, b, gg)
+            if index_dtype == "bf16":
+                hi = wi.round_index_bf16(hi)
             groups[(b, gg)] = (wi.bf16_bits_to_f64(g["K"][b, gg]),
-                               wi.bf16_bits_to_f64(g["V"][b, gg]), gpu_head_index(ix, b, gg))
+                               wi.bf16_bits_to_f64(g["V"][b, gg]), hi)
         Kf, Vf, hi = groups[(b, gg)]
         qf = wi.bf16_bits_to_f64(g["q"][b, h])
         ref = wi.decode_head(qf, Kf, Vf, hi, w.sink, w.window, w.r, dec.scale)

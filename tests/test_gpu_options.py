@@ -1,6 +1,7 @@
 """GPU parity of the decode options against the CPU oracle: the attention-mass
-ranking of the retrieval zone, and speculative reuse of the previous step's
-retrieval sets with the per-KV-head cosine correction.
+ranking of the retrieval zone, speculative reuse of the previous step's
+retrieval sets with the per-KV-head cosine correction, the GQA-shared
+retrieval zone and the bf16 index.
 
 Tolerances as in the plain decode parity: ranking keys within 1e-4 of the
 boundary may swap (the mass key adds ln n_c, computed in f32 on the GPU);
@@ -30,7 +31,7 @@ def lib():
     return wl
 
 
-def compare(dec, g, oidx, r, rank="score", given=None, qbits=None):
+def compare(dec, g, oidx, r, rank="score", given=None, qbits=None, share="head"):
     """Check every head of the decoder's last call against the oracle: heads in
     `given` must have attended over exactly that set; the others over the
     oracle's selection by `rank` (up to ties).  Returns the heads whose GPU
@@ -55,6 +56,16 @@ def compare(dec, g, oidx, r, rank="score", given=None, qbits=None):
                 assert sel.tolist() == want.tolist(), (b, h)
                 ref = wi.decode_head(qf[b, h], Kf[b, gg], Vf[b, gg], hi, cfg.sink, cfg.window, r,
                                      dec.scale, selected=want)
+            elif share == "group":
+                qg = qf[b, gg * group:(gg + 1) * group]
+                want = wi.group_selection(qg, hi["centroid_key"], hi["size"], dec.scale, r, rank)
+                keys = sum(wi.ranking_keys(wi.cluster_scores(x, hi["centroid_key"], hi["size"],
+                                                             dec.scale), hi["size"], rank)
+                           for x in qg)
+                assert len(sel) == len(want)
+                assert sets_match_mod_ties(sel, want, keys, KEY_TOL * group), (b, h)
+                ref = wi.decode_head(qf[b, h], Kf[b, gg], Vf[b, gg], hi, cfg.sink, cfg.window, r,
+                                     dec.scale, selected=sel)
             else:
                 ref = wi.decode_head(qf[b, h], Kf[b, gg], Vf[b, gg], hi, cfg.sink, cfg.window, r,
                                      dec.scale, rank=rank)
@@ -247,3 +258,88 @@ def test_reuse_gap_rows_and_r_zero():
        tau=0.0)
     torch.cuda.synchronize()
     assert d0.status() == 0 and torch.equal(d0.out, plain.out)
+
+
+# ---------------------------------------------------------------- GQA-shared selection
+
+@pytest.mark.parametrize("G,rank", [(1, "score"), (2, "score"), (4, "score"), (8, "score"),
+                                    (4, "mass")])
+def test_shared_selection_parity(G, rank):
+    Hkv = 2
+    g, oidx = random_case(70 + G, B=2, Hq=Hkv * G, Hkv=Hkv, N=6000, sink=4, window=100,
+                          seg_len=1024, k=32, assign_mode="random")
+    ix = gpu_index(g, oidx, 4, 100, 1024, 32)
+    wl = lib()
+    K, V, q = (bf16_tensor(g[n], "cuda") for n in ("K", "V", "q"))
+    r = 11
+    dec = wl.Decoder(ix, Hkv * G, r, rank=rank, share="group")
+    dec(q, K, V)
+    assert dec.status() == 0
+    compare(dec, g, oidx, r, rank=rank, share="group")
+    topk = dec.topk.cpu().numpy()
+    for b in range(2):
+        for gg in range(Hkv):
+            rows = topk[b, gg * G:(gg + 1) * G]
+            assert (rows == rows[0]).all()
+    # each head's scores and maximum are its own
+    sc = dec.scores().cpu().numpy()
+    hm = dec.head_max().cpu().numpy()
+    fin = np.isfinite(sc)
+    np.testing.assert_array_equal(hm, np.where(fin.any(-1), np.where(fin, sc, -np.inf).max(-1),
+                                               -np.inf))
+    if G > 1:
+        per = wl.Decoder(ix, Hkv * G, r, rank=rank)
+        per(q, K, V)
+        torch.cuda.synchronize()
+        assert not torch.equal(per.topk, dec.topk)
+
+
+def test_shared_selection_with_reuse_and_many_clusters():
+    # C = 40448: the group row spans several chunks; then every group reuses
+    # the sets of its first head's previous row
+    Hkv, G = 1, 4
+    g, oidx = random_case(75, B=1, Hq=Hkv * G, Hkv=Hkv, N=40000, sink=4, window=64,
+                          seg_len=512, k=512, assign_mode="random")
+    ix = gpu_index(g, oidx, 4, 64, 512, 512)
+    wl = lib()
+    K, V, q = (bf16_tensor(g[n], "cuda") for n in ("K", "V", "q"))
+    r = 300
+    dec = wl.Decoder(ix, G, r, share="group")
+    dec(q, K, V)
+    assert dec.status() == 0
+    compare(dec, g, oidx, r, share="group")
+    prev = dec.topk[..., :r].clone()
+    prev[0, 1:] = -1  # only the first head's row is read
+    dec(q, K, V, prev_q=q, prev_topk=prev, tau=0.5)
+    assert dec.status() == 0
+    assert dec.reused.cpu().numpy().tolist() == [[1] * G]
+    ids = prev[0, 0].cpu().numpy()
+    ids = ids[ids >= 0]
+    compare(dec, g, oidx, r, given={(0, h): ids for h in range(G)})
+
+
+# ---------------------------------------------------------------- bf16 index
+
+@pytest.mark.parametrize("G,k,share", [(1, 32, "head"), (4, 33, "head"), (8, 64, "head"),
+                                       (4, 32, "group")])
+def test_bf16_index_parity(G, k, share):
+    # k = 33: 3 tiles per group, the last ragged, so stages carry a pair and a
+    # single tile; the oracle decodes against its own bf16 rounding of the
+    # float32 index the GPU holds
+    Hkv = 2
+    g, oidx = random_case(80 + G + k, B=2, Hq=Hkv * G, Hkv=Hkv, N=7000, sink=4, window=100,
+                          seg_len=1024, k=k, assign_mode="random")
+    ix = gpu_index(g, oidx, 4, 100, 1024, k)
+    wl = lib()
+    K, V, q = (bf16_tensor(g[n], "cuda") for n in ("K", "V", "q"))
+    r = 10
+    dec = wl.Decoder(ix, Hkv * G, r, share=share, index_dtype="bf16")
+    ck, vs = dec.index16
+    assert torch.equal(ck, ix.centroid_key.to(torch.bfloat16))
+    assert torch.equal(vs, ix.value_sum.to(torch.bfloat16))
+    dec(q, K, V)
+    assert dec.status() == 0
+    o16 = dict(oidx)
+    for key in ("centroid_key", "value_sum"):
+        o16[key] = ix.tensors[key].double().cpu().numpy()
+    compare(dec, g, wi.round_index_bf16(o16), r, share=share)
