@@ -322,17 +322,68 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.acc)
 
 
-def decode_bytes(w, ix, topk, r):
-    """Algorithmic bytes of one decode step: centroid keys and value sums with
+def decode_bytes(w, ix, topk, r, index_bytes=4):
+    """Algorithmic bytes of one decode step: centroid keys and value sums
+    (index_bytes per element: 4 for the f32 index, 2 for the bf16 one) with
     the sizes, once; steady K/V; retrieved K/V once per (sequence, KV head,
     cluster)."""
     C = w.n_clusters
-    kbar = w.B * w.Hkv * C * (w.d * 4 + 4)
-    vsum = w.B * w.Hkv * C * (w.d * 4 + 4)
+    kbar = w.B * w.Hkv * C * (w.d * index_bytes + 4)
+    vsum = w.B * w.Hkv * C * (w.d * index_bytes + 4)
     steady = w.B * w.Hkv * (w.sink + w.window) * w.d * 2 * 2
     retr = retrieved_unique_bytes(topk[..., :r].contiguous(), ix.size, w.Hq // w.Hkv) if r else 0
     return {"centroid_keys": kbar, "value_sums_sizes": vsum, "steady_kv": steady,
             "retrieved_kv_unique": retr}
+
+
+def measure_variants(w, r, dev, args, pk, flush, ctx):
+    """The decode options on the headline workload's index: attention-mass
+    ranking, GQA-shared selection, the bf16 index (alone and with sharing),
+    and speculative reuse (previous queries equal to the current ones, so
+    every group takes its previous set).  Device time of the fused call per
+    step, each with its own algorithmic bytes and roofline."""
+    import torch
+    import cluster_indexed_sparse_wi_b300 as wl
+    K, V, q, ix = ctx["K"], ctx["V"], ctx["q"], ctx["ix"]
+    stream = torch.cuda.current_stream()
+    hbm_peak = float(pk["hbm_gbs"])
+    out = []
+    variants = (("rank=mass", dict(rank="mass"), {}),
+                ("share=group", dict(share="group"), {}),
+                ("index=bf16", dict(index_dtype="bf16"), {}),
+                ("share=group,index=bf16", dict(share="group", index_dtype="bf16"), {}),
+                ("reuse(tau=0.9)", {}, dict(tau=0.9)))
+    for name, opts, call in variants:
+        dec = wl.Decoder(ix, w.Hq, r, **opts)
+        dec(q, K, V)
+        torch.cuda.synchronize()
+        if call:
+            prev = dec.topk[..., :r].clone()
+            fn = lambda: dec(q, K, V, with_topk=True, prev_q=q, prev_topk=prev, **call)
+        else:
+            fn = lambda: dec(q, K, V, with_topk=False)
+        for _ in range(max(args.warmup, 3)):
+            flush()
+            fn()
+        gr = wl.capture_graph(fn, dev)
+        for _ in range(3):
+            flush()
+            gr.replay()
+        step_ms = timed_steps(gr.replay, flush, args.steps, stream)
+        assert dec.status() == 0
+        dec(q, K, V, with_topk=True, **({} if not call else dict(prev_q=q, prev_topk=prev, **call)))
+        torch.cuda.synchronize()
+        by = decode_bytes(w, ix, dec.topk, r, index_bytes=2 if "bf16" in name else 4)
+        ms = statistics.mean(step_ms)
+        gbs = sum(by.values()) / (ms * 1e-3) / 1e9
+        out.append({"variant": name, "ms_per_step": ms, "value": w.B / (ms * 1e-3), "unit": UNIT,
+                    "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": gbs,
+                                 "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                                 "algorithmic_bytes_per_launch": sum(by.values())},
+                    "bytes": by,
+                    "reused_heads": int(dec.reused.sum()) if call else None})
+        del dec, gr
+    return out
 
 
 def timed_steps(fn, flush, steps, stream):
@@ -579,6 +630,14 @@ def main():
         val, desc, _ = oracle_decode_sample(w, g_np, index_np, r, args.cpu_seconds)
         cpu = {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": desc, "host_cpus": os.cpu_count()}
+    # ---- the decode options on the headline index
+    variants = []
+    if not args.no_sweep and ws == 1:
+        try:
+            variants = measure_variants(w, r, dev, args, pk, flush, ctx)
+        except Exception as e:  # report, keep the headline
+            variants = [{"error": str(e)[:300]}]
+
     del ctx, K, V, q, ix, dec, g_np
     torch.cuda.empty_cache()
 
@@ -642,6 +701,7 @@ def main():
         "build": build,
         "full_pass_ms": (build["ms"] + ms) if build else None,
         "sweep": sweep,
+        "variants": variants,
         "wall_s_timed_region_1": res["wall_s_timed"],
         "setup_seconds": res["setup_seconds"],
     }

@@ -59,6 +59,7 @@ __all__ = [
     "index_statistics",
     "build_index_head",
     "build_index",
+    "extend_index_head",
     "cluster_scores",
     "select_clusters",
     "ranking_keys",
@@ -254,6 +255,51 @@ def build_index_head(K: np.ndarray, V: np.ndarray, sink: int, window: int, seg_l
         mu[s * k_per_seg:(s + 1) * k_per_seg] = m
         assign[pos] = s * k_per_seg + a
     idx = np.arange(sink, N - window, dtype=np.int64)
+    st = index_statistics(K, V, idx, assign[idx], C)
+    st["unit_centroid"] = mu
+    st["assign"] = assign
+    st["n_clusters"] = C
+    return st
+
+
+def extend_index_head(K: np.ndarray, V: np.ndarray, old: Dict[str, np.ndarray], N_old: int,
+                      sink: int, window: int, seg_len: int,
+                      k_per_seg: int) -> Dict[str, np.ndarray]:
+    """Index maintenance during decode (RetroInfer summary §2.A.1: the local
+    window slides, so its oldest tokens leave the steady zone).  The context
+    grew from N_old to N = K.shape[0] positions; the positions
+    [N_old - window, N - window) leave the window and join the index without
+    re-clustering.
+
+    Readings (the pages are silent on maintenance):
+    * every earlier position keeps its cluster, and the unit centroids are
+      kept (clusters of segments that appear only now start empty, with zero
+      centroids, as an empty segment's do at build time);
+    * a joining position p goes to the nearest unit centroid,
+      argmax_j k_p . mu_j with the lowest j among equal maxima, of its own
+      segment p // seg_len when that segment held indexable positions
+      before, else of the last segment that did (a new segment is opened only
+      by re-clustering, i.e. a rebuild);
+    * sizes, mean keys, value sums and the sorted copies are then those of
+      the new assignment (``index_statistics``)."""
+    N, d = K.shape
+    segs_old = segment_positions(N_old, sink, window, seg_len)
+    clustered = [s for s, pos in enumerate(segs_old) if pos.size > 0]
+    if not clustered:
+        raise ValueError("the earlier index holds no clustered segment")
+    last = clustered[-1]
+    C = -(-N // seg_len) * k_per_seg
+    mu = np.zeros((C, d))
+    C_old = old["unit_centroid"].shape[0]
+    mu[:C_old] = old["unit_centroid"]
+    assign = np.full(N, -1, dtype=np.int64)
+    lo, hi_old, hi = sink, N_old - window, N - window
+    assign[lo:hi_old] = old["assign"][lo:hi_old]
+    for p in range(max(hi_old, lo), hi):
+        s = min(p // seg_len, last)
+        a, _ = kmeans_assign(K[p:p + 1], mu[s * k_per_seg:(s + 1) * k_per_seg])
+        assign[p] = s * k_per_seg + a[0]
+    idx = np.arange(sink, hi, dtype=np.int64)
     st = index_statistics(K, V, idx, assign[idx], C)
     st["unit_centroid"] = mu
     st["assign"] = assign

@@ -606,3 +606,63 @@ def test_shared_decode_reduces_and_extends_per_head_decode():
     assert differs > 0
     with pytest.raises(ValueError):
         wi.decode(q, K, V, idx, z["sink"], z["window"], 5, 0.2, share="pair")
+
+
+# ---------------------------------------------------------------- index maintenance
+
+def test_extend_by_nothing_is_the_identity():
+    K, V, q, idx = small_case(seed=50, d=32)
+    N = K.shape[0]
+    ext = wi.extend_index_head(K, V, idx, N, 4, 32, 256, 16)
+    for key in ("size", "offset", "perm", "assign", "centroid_key", "value_sum", "k_sorted",
+                "v_sorted", "unit_centroid"):
+        np.testing.assert_array_equal(ext[key], idx[key], err_msg=key)
+
+
+def test_extend_assigns_joining_tokens_by_bruteforce_nearest_centroid():
+    # a 700-token index grown to 760: the 60 positions that leave the window
+    # are [668, 728); explicit loops over each one's segment centroids (ties
+    # to the lower j) give its cluster; earlier positions keep theirs
+    rng = np.random.default_rng(51)
+    N0, N1, d, sink, window, L, k = 700, 760, 16, 4, 32, 256, 8
+    K = bf16_vals(rng, (N1, d))
+    V = bf16_vals(rng, (N1, d))
+    old = wi.build_index_head(K[:N0], V[:N0], sink, window, L, k, 3)
+    ext = wi.extend_index_head(K, V, old, N0, sink, window, L, k)
+    mu = old["unit_centroid"]
+    np.testing.assert_array_equal(ext["assign"][:N0 - window], old["assign"][:N0 - window])
+    for p in range(N0 - window, N1 - window):
+        s = p // L
+        best, arg = -np.inf, -1
+        for j in range(k):
+            v = float(sum(K[p, t] * mu[s * k + j, t] for t in range(d)))
+            if v > best:
+                best, arg = v, j
+        assert ext["assign"][p] == s * k + arg, p
+    assert np.all(ext["assign"][N1 - window:] == -1) and np.all(ext["assign"][:sink] == -1)
+    # statistics of the new assignment: every indexable position once
+    assert ext["size"].sum() == N1 - window - sink
+    assert sorted(ext["perm"].tolist()) == list(range(sink, N1 - window))
+
+
+def test_extend_past_the_last_segment_and_centroid_directions():
+    # N0 = 300 with seg_len 256: the clustered segments are 0 and 1 (1 holds
+    # [256, 284)); growing to 600 makes positions up to 584 join, those of
+    # segment 2 go to segment 1's clusters; a token along a centroid's
+    # direction joins that centroid's cluster; segment 2's clusters stay empty
+    rng = np.random.default_rng(52)
+    N0, N1, d, sink, window, L, k = 300, 600, 8, 4, 16, 256, 4
+    K = bf16_vals(rng, (N1, d))
+    V = bf16_vals(rng, (N1, d))
+    old = wi.build_index_head(K[:N0], V[:N0], sink, window, L, k, 2)
+    mu = old["unit_centroid"]
+    K[550] = 3.0 * mu[k + 2]  # segment 2 position, along segment 1's centroid 2
+    ext = wi.extend_index_head(K, V, old, N0, sink, window, L, k)
+    assert ext["n_clusters"] == 3 * k
+    assert ext["assign"][550] == k + 2
+    seg2 = np.arange(512, N1 - window)
+    assert np.all((ext["assign"][seg2] >= k) & (ext["assign"][seg2] < 2 * k))
+    assert np.all(ext["size"][2 * k:] == 0) and np.all(ext["unit_centroid"][2 * k:] == 0)
+    with pytest.raises(ValueError):
+        wi.extend_index_head(K, V, {"unit_centroid": np.zeros((k, d)), "assign": np.full(20, -1)},
+                             20, 4, 16, L, k)
