@@ -30,7 +30,8 @@ FIELDS = ["centroid_key", "unit_centroid", "value_sum", "size", "offset", "perm"
 
 # C ABI entry points, in header order (tests check the header against this).
 SYMBOLS = [
-    "wi_index_sizes", "wi_build_workspace_bytes", "wi_build_index", "wi_build_init",
+    "wi_index_sizes", "wi_build_workspace_bytes", "wi_build_index", "wi_index_extend",
+    "wi_build_init",
     "wi_kmeans_assign", "wi_kmeans_update", "wi_build_finalize", "wi_decode_workspace_bytes",
     "wi_decode_workspace_layout", "wi_decode_attention", "wi_index_round_bf16",
     "wi_decode_attention_ex",
@@ -107,6 +108,7 @@ def lib() -> ctypes.CDLL:
         "wi_index_sizes": (i, [bp, P(sz)]),
         "wi_build_workspace_bytes": (sz, [bp]),
         "wi_build_index": (i, [bp, vp, vp, ip, vp, sz, vp]),
+        "wi_index_extend": (i, [bp, vp, vp, ip, ip, vp, sz, vp]),
         "wi_build_init": (i, [bp, vp, ip, vp, sz, vp]),
         "wi_kmeans_assign": (i, [bp, vp, ip, vp, sz, vp]),
         "wi_kmeans_update": (i, [bp, vp, ip, vp, sz, vp]),

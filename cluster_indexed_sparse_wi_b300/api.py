@@ -173,6 +173,22 @@ class WaveIndex:
     def status(self, stream=None) -> int:
         return sync_status(self.workspace, stream)
 
+    def extended(self, K, V, stream=None) -> "WaveIndex":
+        """The index of the grown context K, V [B, Hkv, N', d] (N' >= N):
+        positions that left the local window join their segment's nearest
+        unit centroid, earlier positions keep their clusters
+        (wi_index_extend).  Returns a new WaveIndex; this one is unchanged."""
+        c = self.cfg
+        N1 = K.shape[2]
+        cfg = dataclasses.replace(c, N=N1)
+        new = WaveIndex(cfg, self.device)
+        new._kv(K, V)
+        L.check(L.lib().wi_index_extend(ctypes.byref(cfg.params()), _ptr(K), _ptr(V),
+                                        ctypes.byref(self.struct), ctypes.byref(new.struct),
+                                        _ptr(new.workspace), new.workspace.numel(),
+                                        _stream(stream)), "wi_index_extend")
+        return new
+
     def round_bf16(self, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
         """bf16 copies (round to nearest even) of the mean keys and value
         sums: the leaner index a Decoder with index_dtype="bf16" streams."""

@@ -514,6 +514,53 @@ int wi_build_finalize(const wi_build_params* p, const void* K, const void* V, wi
   return cuda_status(e);
 }
 
+int wi_index_extend(const wi_build_params* p, const void* K, const void* V,
+                    const wi_index* old_index, wi_index* index, void* workspace,
+                    size_t workspace_bytes, wi_stream_t stream) {
+  if (old_index == nullptr) return WI_ERR_INVALID_ARG;
+  BuildArgs a;
+  int st = fill_build_args(p, K, V, index, workspace, workspace_bytes, &a);
+  if (st != WI_OK) return st;
+  if ((st = check_index_ptrs(a, kNeedInit | kNeedAssign | kNeedUpdate | kNeedFinal)) != WI_OK)
+    return st;
+  const wi_index* o = old_index;
+  if (o->B != p->B || o->Hkv != p->Hkv || o->d != p->d || o->sink != p->sink ||
+      o->window != p->window || o->seg_len != p->seg_len || o->k_per_seg != p->k_per_seg ||
+      o->N > p->N || o->n_clusters <= 0)
+    return WI_ERR_INDEX_MISMATCH;
+  if (o->unit_centroid == nullptr || o->assign == nullptr) return WI_ERR_INVALID_ARG;
+  if (!aligned(o->unit_centroid, 16) || !aligned(o->assign, 16)) return WI_ERR_ALIGNMENT;
+  // the joining positions must lie in segments the earlier index clustered
+  const int hi_old = o->N - o->window;
+  if (hi_old <= o->sink) return WI_ERR_UNSUPPORTED;
+  const int s_last = (hi_old - 1) / p->seg_len;
+  if ((long long)p->N - p->window > (long long)(s_last + 1) * p->seg_len) return WI_ERR_UNSUPPORTED;
+  if ((st = device_ok()) != WI_OK) return st;
+  wi::ExtendArgs e;
+  e.B = p->B;
+  e.Hkv = p->Hkv;
+  e.N0 = o->N;
+  e.N1 = p->N;
+  e.sink = p->sink;
+  e.window = p->window;
+  e.L = p->seg_len;
+  e.k = p->k_per_seg;
+  e.C_old = o->n_clusters;
+  e.C_new = a.C;
+  e.s_last = s_last;
+  e.K = a.K;
+  e.mu_old = static_cast<const uint16_t*>(o->unit_centroid);
+  e.assign_old = o->assign;
+  e.mu_new = a.mu;
+  e.assign_new = a.assign;
+  record(p, index);
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t err = wi::launch_extend(e, s);
+  if (err == cudaSuccess) err = wi::launch_cluster_sort(a, s);
+  if (err == cudaSuccess) err = wi::launch_finalize_stats(a, s);
+  return cuda_status(err);
+}
+
 int wi_build_index(const wi_build_params* p, const void* K, const void* V, wi_index* index,
                    void* workspace, size_t workspace_bytes, wi_stream_t stream) {
   BuildArgs a;

@@ -15,6 +15,11 @@
 //   finalize_kernel       : mean key, value sum, cluster-sorted K/V copies.
 //   round_bf16_kernel     : bf16 copies of the mean keys and value sums (the
 //                           leaner index decode may stream instead).
+//   extend_copy_kernel /  : index maintenance as the local window slides:
+//   extend_assign_kernel    earlier assignments and centroids carried over,
+//                           each joining position to its segment's nearest
+//                           unit centroid (then the sort and statistics
+//                           kernels above on the new assignment).
 #include "wi_device.cuh"
 #include "wi_internal.h"
 
@@ -288,6 +293,84 @@ __global__ void round_bf16_kernel(const float4* __restrict__ src, uint2* __restr
     dst[i] = make_uint2((uint32_t)f2bf(v.x) | ((uint32_t)f2bf(v.y) << 16),
                         (uint32_t)f2bf(v.z) | ((uint32_t)f2bf(v.w) << 16));
   }
+}
+
+// Carried-over state of one (sequence, KV head): unit centroids (zero for
+// clusters new to the index), assignments of the earlier indexable positions,
+// -1 on the steady zone.  Joining positions are left to extend_assign_kernel.
+__global__ void extend_copy_kernel(ExtendArgs e) {
+  const int bh = blockIdx.y;
+  const size_t mu_words = (size_t)e.C_new * kD / 2;  // bf16 pairs
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(e.mu_old) + (size_t)bh * e.C_old * kD / 2;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(e.mu_new) + (size_t)bh * mu_words;
+  const size_t old_words = (size_t)e.C_old * kD / 2;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < mu_words;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = i < old_words ? src[i] : 0u;
+  const int hi_old = e.N0 - e.window, hi = e.N1 - e.window;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < e.N1; p += gridDim.x * blockDim.x) {
+    if (p >= hi_old && p < hi && p >= e.sink) continue;  // joining: extend_assign_kernel
+    const bool idx = p >= e.sink && p < hi_old;
+    e.assign_new[(size_t)bh * e.N1 + p] = idx ? e.assign_old[(size_t)bh * e.N0 + p] : -1;
+  }
+}
+
+// One warp per joining position: a(p) = t k + argmax_j k_p . mu_{t k + j}
+// (f32 sums of bf16 products, the lowest j among equal maxima), t = p / L,
+// the position's segment (clustered before: the host checks it).
+__global__ void __launch_bounds__(256) extend_assign_kernel(ExtendArgs e, int n_join) {
+  __shared__ float keys[8][kD];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const long long gw = (long long)blockIdx.x * 8 + w;
+  const int bh = (int)(gw / n_join);
+  if (bh >= e.B * e.Hkv) return;
+  const int p = max(e.N0 - e.window, e.sink) + (int)(gw - (long long)bh * n_join);
+  const uint2 kw = *reinterpret_cast<const uint2*>(e.K + ((size_t)bh * e.N1 + p) * kD + lane * 4);
+  keys[w][lane * 4] = bf_lo(kw.x);
+  keys[w][lane * 4 + 1] = bf_hi(kw.x);
+  keys[w][lane * 4 + 2] = bf_lo(kw.y);
+  keys[w][lane * 4 + 3] = bf_hi(kw.y);
+  __syncwarp();
+  const int t = p / e.L;
+  const uint16_t* mu = e.mu_old + ((size_t)bh * e.C_old + (size_t)t * e.k) * kD;
+  float best = -INFINITY;
+  int arg = 0x7fffffff;
+  for (int j = lane; j < e.k; j += 32) {
+    const uint2* row = reinterpret_cast<const uint2*>(mu + (size_t)j * kD);
+    float acc = 0.f;
+#pragma unroll 8
+    for (int q = 0; q < kD / 4; ++q) {
+      const uint2 m = row[q];
+      acc = fmaf(keys[w][4 * q], bf_lo(m.x), acc);
+      acc = fmaf(keys[w][4 * q + 1], bf_hi(m.x), acc);
+      acc = fmaf(keys[w][4 * q + 2], bf_lo(m.y), acc);
+      acc = fmaf(keys[w][4 * q + 3], bf_hi(m.y), acc);
+    }
+    if (acc > best) {  // j ascends within the lane: the first maximum is kept
+      best = acc;
+      arg = j;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(kFull, best, o);
+    const int oa = __shfl_xor_sync(kFull, arg, o);
+    if (ob > best || (ob == best && oa < arg)) {
+      best = ob;
+      arg = oa;
+    }
+  }
+  if (lane == 0) e.assign_new[(size_t)bh * e.N1 + p] = t * e.k + (arg < e.k ? arg : 0);
+}
+
+cudaError_t launch_extend(const ExtendArgs& e, cudaStream_t st) {
+  extend_copy_kernel<<<dim3(16, e.B * e.Hkv), 256, 0, st>>>(e);
+  cudaError_t err = cudaGetLastError();
+  const int n_join = (e.N1 - e.window) - max(e.N0 - e.window, e.sink);
+  if (err != cudaSuccess || n_join <= 0) return err;
+  const long long warps = (long long)e.B * e.Hkv * n_join;
+  extend_assign_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(e, n_join);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_round_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st) {

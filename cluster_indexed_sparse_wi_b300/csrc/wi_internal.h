@@ -162,6 +162,18 @@ cudaError_t launch_kmeans_assign(const BuildArgs& a, cudaStream_t st);
 cudaError_t launch_cluster_sort(const BuildArgs& a, cudaStream_t st);
 cudaError_t launch_centroid_update(const BuildArgs& a, cudaStream_t st);
 cudaError_t launch_finalize_stats(const BuildArgs& a, cudaStream_t st);
+// Index maintenance: the context grew from N0 to N1 positions; positions
+// [N0 - window, N1 - window) join the index (wi_build.cu).
+struct ExtendArgs {
+  int B, Hkv, N0, N1, sink, window, L, k, C_old, C_new, s_last;
+  const uint16_t* K;         // bf16 [B,Hkv,N1,128]
+  const uint16_t* mu_old;    // bf16 [B,Hkv,C_old,128]
+  const int* assign_old;     // [B,Hkv,N0]
+  uint16_t* mu_new;          // bf16 [B,Hkv,C_new,128]
+  int* assign_new;           // [B,Hkv,N1]
+};
+cudaError_t launch_extend(const ExtendArgs& e, cudaStream_t st);
+
 // dst[i] = bf16(src[i]) for i < n (n a multiple of 4; 16-byte aligned arrays)
 cudaError_t launch_round_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st);
 

@@ -150,6 +150,27 @@ WI_API size_t wi_build_workspace_bytes(const wi_build_params *p);
 WI_API int wi_build_index(const wi_build_params *p, const void *K, const void *V, wi_index *index,
                    void *workspace, size_t workspace_bytes, wi_stream_t stream);
 
+/* Index maintenance as the local window slides (technical summary (es)
+ * §2.A.1; the pages give no maintenance rule, this is the reading): the
+ * context grew from old_index->N to p->N positions, so positions
+ * [old N - window, p->N - window) leave the steady zone and join the index
+ * without re-clustering.  Earlier positions keep their clusters and the unit
+ * centroids are carried over (clusters of segments new to the index start
+ * empty with zero centroids); a joining position p takes the nearest unit
+ * centroid of its segment, argmax_j k_p . mu_j (f32 sums, the lowest j among
+ * equal maxima); then size / offset / perm, mean keys, value sums and the
+ * sorted copies are those of the new assignment (as wi_build_finalize).
+ * p: the build parameters of the grown context (same B, Hkv, sink, window,
+ * seg_len, k_per_seg as old_index; iters unused).  K, V: bf16 [B,Hkv,p->N,d].
+ * index: arrays sized by wi_index_sizes(p), not shared with old_index.
+ * workspace: wi_build_workspace_bytes(p).  WI_ERR_INDEX_MISMATCH when the
+ * shapes differ or the context shrank; WI_ERR_UNSUPPORTED when a joining
+ * position falls in a segment the earlier index did not cluster (or it
+ * clustered none): a rebuild opens that segment. */
+WI_API int wi_index_extend(const wi_build_params *p, const void *K, const void *V,
+                    const wi_index *old_index, wi_index *index, void *workspace,
+                    size_t workspace_bytes, wi_stream_t stream);
+
 /* Build step 1: key norms ||k_i|| (f32, into the workspace), assign = -1 on
  * the steady zone, and the initial centroids: with the m_s indexable keys of
  * segment s in position order, centroid j = bf16(k_p / ||k_p||) for

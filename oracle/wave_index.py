@@ -277,9 +277,9 @@ def extend_index_head(K: np.ndarray, V: np.ndarray, old: Dict[str, np.ndarray], 
       centroids, as an empty segment's do at build time);
     * a joining position p goes to the nearest unit centroid,
       argmax_j k_p . mu_j with the lowest j among equal maxima, of its own
-      segment p // seg_len when that segment held indexable positions
-      before, else of the last segment that did (a new segment is opened only
-      by re-clustering, i.e. a rebuild);
+      segment p // seg_len, which must have held indexable positions before
+      (ValueError otherwise: a segment without centroids is opened by
+      re-clustering, i.e. a rebuild);
     * sizes, mean keys, value sums and the sorted copies are then those of
       the new assignment (``index_statistics``)."""
     N, d = K.shape
@@ -288,6 +288,8 @@ def extend_index_head(K: np.ndarray, V: np.ndarray, old: Dict[str, np.ndarray], 
     if not clustered:
         raise ValueError("the earlier index holds no clustered segment")
     last = clustered[-1]
+    if N - window > (last + 1) * seg_len:
+        raise ValueError("joining positions reach a segment without centroids")
     C = -(-N // seg_len) * k_per_seg
     mu = np.zeros((C, d))
     C_old = old["unit_centroid"].shape[0]
@@ -296,7 +298,7 @@ def extend_index_head(K: np.ndarray, V: np.ndarray, old: Dict[str, np.ndarray], 
     lo, hi_old, hi = sink, N_old - window, N - window
     assign[lo:hi_old] = old["assign"][lo:hi_old]
     for p in range(max(hi_old, lo), hi):
-        s = min(p // seg_len, last)
+        s = p // seg_len
         a, _ = kmeans_assign(K[p:p + 1], mu[s * k_per_seg:(s + 1) * k_per_seg])
         assign[p] = s * k_per_seg + a[0]
     idx = np.arange(sink, hi, dtype=np.int64)

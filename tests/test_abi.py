@@ -205,3 +205,31 @@ def test_decode_option_validation(L):
     assert lib.wi_decode_attention_ex(ctypes.byref(dp(L)), None, fake, fake, fake,
                                       ctypes.byref(ix), fake, None, None, fake, 1 << 30,
                                       None) == L.WI_ERR_INDEX_MISMATCH
+
+
+def test_index_extend_host_checks(L):
+    # shapes must match the earlier index; the context may not shrink; joining
+    # positions must stay in segments the earlier index clustered
+    lib = L.lib()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def ix(N):
+        t = L.IndexStruct()
+        for name in L.FIELDS:
+            setattr(t, name, 1 << 20)
+        t.B, t.Hkv, t.N, t.d, t.sink, t.window, t.seg_len, t.k_per_seg = 1, 2, N, 128, 4, 64, 1024, 32
+        t.n_clusters = -(-N // 1024) * 32
+        return t
+
+    def call(N1, old, **kw):
+        p = bp(L, N=N1, seg_len=1024, k_per_seg=32, window=64, **kw)
+        new = ix(N1)
+        return lib.wi_index_extend(ctypes.byref(p), fake, fake, ctypes.byref(old),
+                                   ctypes.byref(new), fake, 1 << 30, None)
+
+    assert call(3000, ix(3100)) == L.WI_ERR_INDEX_MISMATCH     # shrank
+    assert call(3000, ix(2900), sink=5) == L.WI_ERR_INDEX_MISMATCH
+    assert call(3200, ix(3000)) == L.WI_ERR_UNSUPPORTED        # [2936, 3136) reaches segment 3
+    assert call(3000, ix(40)) == L.WI_ERR_UNSUPPORTED          # nothing clustered before
+    assert lib.wi_index_extend(ctypes.byref(bp(L)), fake, fake, None, ctypes.byref(ix(3000)),
+                               fake, 1 << 30, None) == L.WI_ERR_INVALID_ARG

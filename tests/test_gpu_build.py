@@ -214,3 +214,70 @@ def test_full_size_build_segment_agreement():
     agree = float(np.mean(a_gpu == a_ref))
     print("128K segment assignment agreement", agree)
     assert agree >= 0.999
+
+
+def test_extend_matches_oracle_and_decodes():
+    # Index maintenance: a 9000-position index (3 segments of 4096) grown to
+    # 12400 positions; [8700, 12100) leave the window and join segment 2's
+    # clusters; the index gains an empty fourth segment.  The oracle extends
+    # the GPU's own earlier index (its centroids and assignment).
+    import cluster_indexed_sparse_wi_b300 as wl
+    from tests._util import head_index, index_to_numpy, rel_err
+    c = dict(B=1, Hkv=2, N=12400, sink=4, window=300, seg_len=4096, k=64, iters=3)
+    w = WORKLOADS["llama3_8b_128k_b1"].replace(
+        B=1, Hq=8, Hkv=2, N=c["N"], sink=4, window=300, seg_len=4096, k_per_seg=64, iters=3,
+        planted_per_seg=32, seeds=(17,))
+    g = generate(w)
+    N0 = 9000
+    K1, V1 = bf16_tensor(g["K"], "cuda"), bf16_tensor(g["V"], "cuda")
+    K0, V0 = K1[:, :, :N0].contiguous(), V1[:, :, :N0].contiguous()
+    cfg0 = wl.IndexConfig(1, 2, N0, 4, 300, 4096, 64, 3)
+    old = wl.WaveIndex(cfg0, "cuda").build(K0, V0)
+    new = old.extended(K1, V1)
+    torch.cuda.synchronize()
+    assert old.status() == 0 and new.status() == 0
+    assert new.cfg.n_clusters == 4 * 64
+    Kf, Vf = f64(g["K"]), f64(g["V"])
+    a_new = dl(new.assign)
+    o_np = index_to_numpy(old)
+    ties = 0
+    for h in range(2):
+        old_h = {"unit_centroid": o_np["unit_centroid"][0, h], "assign": o_np["assign"][0, h]}
+        ref = wi.extend_index_head(Kf[0, h], Vf[0, h], old_h, N0, 4, 300, 4096, 64)
+        assert np.array_equal(a_new[0, h, :N0 - 300], ref["assign"][:N0 - 300])
+        join = np.arange(N0 - 300, c["N"] - 300)
+        got, want = a_new[0, h, join], ref["assign"][join]
+        assert np.all(got // 64 == 2)
+        mu = o_np["unit_centroid"][0, h, 128:192]
+        bad = np.nonzero(got != want)[0]
+        if bad.size:
+            _, cos = wi.kmeans_assign(Kf[0, h][join[bad]], mu)
+            gap = np.abs(cos[np.arange(bad.size), got[bad] - 128] -
+                         cos[np.arange(bad.size), want[bad] - 128])
+            assert np.all(gap < COS_TIE)
+            ties += bad.size
+            continue  # statistics follow the GPU's assignment; checked below
+        assert np.array_equal(dl(new.size)[0, h], ref["size"])
+        assert np.array_equal(dl(new.offset)[0, h], ref["offset"])
+        assert np.array_equal(dl(new.perm)[0, h], ref["perm"])
+        for name in ("centroid_key", "value_sum"):
+            got_s = dl(new.tensors[name])[0, h]
+            scale = np.abs(ref[name]).max(axis=1, keepdims=True) + 1e-6
+            assert np.all(np.abs(got_s - ref[name]) <= 1e-5 * scale), name
+        assert np.array_equal(dl(new.k_sorted)[0, h], ref["k_sorted"])
+        assert np.array_equal(dl(new.unit_centroid)[0, h], ref["unit_centroid"])
+    print("extension assignment ties", ties)
+    # the extended index decodes like the oracle's tripartite attention over it
+    q = bf16_tensor(g["q"], "cuda")
+    dec = wl.Decoder(new, 8, 20)
+    out, lse, topk = dec(q, K1, V1)
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    n_np = index_to_numpy(new)
+    qf = f64(g["q"])
+    for h in (0, 5):
+        hi = head_index(n_np, 0, h // 4)
+        sel = topk[0, h].cpu().numpy()
+        ref = wi.decode_head(qf[0, h], Kf[0, h // 4], Vf[0, h // 4], hi, 4, 300, 20, dec.scale,
+                             selected=sel[sel >= 0])
+        assert rel_err(out[0, h].cpu().numpy(), ref["out"]) <= 1e-2

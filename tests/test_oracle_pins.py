@@ -645,24 +645,26 @@ def test_extend_assigns_joining_tokens_by_bruteforce_nearest_centroid():
     assert sorted(ext["perm"].tolist()) == list(range(sink, N1 - window))
 
 
-def test_extend_past_the_last_segment_and_centroid_directions():
-    # N0 = 300 with seg_len 256: the clustered segments are 0 and 1 (1 holds
-    # [256, 284)); growing to 600 makes positions up to 584 join, those of
-    # segment 2 go to segment 1's clusters; a token along a centroid's
-    # direction joins that centroid's cluster; segment 2's clusters stay empty
+def test_extend_within_the_last_segment_and_centroid_directions():
+    # N0 = 300, window 16, seg_len 256: the clustered segments are 0 and 1 (1
+    # holds [256, 284)); growing to 520 makes [284, 504) join segment 1 and
+    # opens segment 2 on the index side (its clusters stay empty, zero
+    # centroids); a token along a centroid's direction joins that centroid's
+    # cluster; growing to 600 would reach into segment 2: a rebuild
     rng = np.random.default_rng(52)
-    N0, N1, d, sink, window, L, k = 300, 600, 8, 4, 16, 256, 4
-    K = bf16_vals(rng, (N1, d))
-    V = bf16_vals(rng, (N1, d))
+    N0, d, sink, window, L, k = 300, 8, 4, 16, 256, 4
+    K = bf16_vals(rng, (700, d))
+    V = bf16_vals(rng, (700, d))
     old = wi.build_index_head(K[:N0], V[:N0], sink, window, L, k, 2)
     mu = old["unit_centroid"]
-    K[550] = 3.0 * mu[k + 2]  # segment 2 position, along segment 1's centroid 2
-    ext = wi.extend_index_head(K, V, old, N0, sink, window, L, k)
+    K[400] = mu[k + 2] * 4.0  # a power of two keeps it a bf16 value
+    ext = wi.extend_index_head(K[:520], V[:520], old, N0, sink, window, L, k)
     assert ext["n_clusters"] == 3 * k
-    assert ext["assign"][550] == k + 2
-    seg2 = np.arange(512, N1 - window)
-    assert np.all((ext["assign"][seg2] >= k) & (ext["assign"][seg2] < 2 * k))
+    assert ext["assign"][400] == k + 2
+    assert np.all((ext["assign"][256:504] >= k) & (ext["assign"][256:504] < 2 * k))
     assert np.all(ext["size"][2 * k:] == 0) and np.all(ext["unit_centroid"][2 * k:] == 0)
     with pytest.raises(ValueError):
-        wi.extend_index_head(K, V, {"unit_centroid": np.zeros((k, d)), "assign": np.full(20, -1)},
-                             20, 4, 16, L, k)
+        wi.extend_index_head(K[:600], V[:600], old, N0, sink, window, L, k)
+    with pytest.raises(ValueError):
+        wi.extend_index_head(K[:30], V[:30], {"unit_centroid": np.zeros((k, d)),
+                                              "assign": np.full(20, -1)}, 20, 4, 16, L, k)
