@@ -2270,7 +2270,10 @@ __device__ void signaler(const DecodeArgs& a, DecSmem& S) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+// 96 registers: 18 warps, up to 5 per SM sub-partition, fit its 16K registers.
+// (A per-kernel register limit instead of launch bounds: the same limit
+// without the spills the launch-bounds heuristics leave.)
+__global__ void __maxnreg__(96) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecSmem& S = *reinterpret_cast<DecSmem*>(smem_raw);
   const int tid = threadIdx.x;
