@@ -1238,6 +1238,7 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
   uint32_t seq = 0;
   bool inject = a.inject != 0, skipped = false;
   const int ns = a.sink + a.window;
+  const uint64_t stream_policy = l2_evict_first();  // every staged byte is read once per call
   const long long H = (long long)a.B * a.Hq;
 
   // claim the next ring slot (warp-uniform); false once this block aborted
@@ -1269,7 +1270,7 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
   };
   auto copy_to = [&](void* dst, const void* src, uint32_t bytes, int stage) {
     if (inject) skipped = true;
-    else bulk_g2s(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]));
+    else bulk_g2s_hint(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]), stream_policy);
   };
 
   // 1-2. index and steady tiles: lane 0 alone, addresses advanced
@@ -1287,7 +1288,7 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
       return true;
     };
     auto issue = [&](void* dst, const void* src, uint32_t bytes, int stage) {
-      if (!inj) bulk_g2s(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]));
+      if (!inj) bulk_g2s_hint(smem_addr(dst), src, bytes, smem_addr(&S.full[stage]), stream_policy);
     };
     auto done_tile = [&]() {
       inj = false;  // the test hook drops the copies of the first tile only

@@ -141,6 +141,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// The same copy with an L2 eviction-policy hint (see l2_evict_first).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+// L2 policy for data read once per call: its lines are the first evicted, so
+// streaming it does not push out other lines (dirty ones included, whose
+// eviction costs a write-back).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 // Orders this thread's earlier generic-proxy accesses of global memory (here:
 // the acquire that saw other blocks' writes) before its later bulk copies.
 __device__ __forceinline__ void fence_proxy_async_global() {
