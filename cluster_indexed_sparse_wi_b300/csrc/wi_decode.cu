@@ -18,12 +18,17 @@
 //           for the group's G query heads -> scores (global) and a copy of
 //           the block's own scores in shared memory;
 //        b. the selections assigned to this block and round: once the head's
-//           KV group is fully scored, the r largest scores (ties to the lower
-//           id), their clusters' sorted rows, sizes, token offsets and scores;
+//           KV group is fully scored, the r largest ranking keys (ties to the
+//           lower id), their clusters' sorted rows, sizes, token offsets and
+//           scores;
 //        c. value-sum tiles of the same clusters: the estimate of every
 //           non-empty cluster from the block's own scores,
 //           (m, l = sum n_c e^{s_c - m}, o = sum e^{s_c - m} vsum_c), one
 //           partial per (chunk, KV group, query head);
+//      with few heads over several rounds (a.kbar_first) the centroid-key
+//      tiles of every round come first, then every selection, then the
+//      value-sum tiles (last round first; earlier rounds' scores are read
+//      back from global memory);
 //   2. its steady-zone tiles (sink and local-window K/V rows of one KV group,
 //      the group's G query heads at once), exact attention, one partial per
 //      (tile, head);
@@ -51,8 +56,15 @@
 // only at points fixed by the static schedule, which every consumer warp
 // passes whether or not a wait of it gave up.
 //
-// Softmax quantities are kept in log2 units (logits scaled by log2 e) so that
-// every exponential is an exp2.
+// Every staged byte is read once per call, so the copies carry an L2
+// evict-first policy.  Softmax quantities are kept in log2 units (logits
+// scaled by log2 e) so that every exponential is an exp2.
+//
+// Options (wi_decode_options): the ranking key may be the attention mass
+// s_c + ln n_c; a KV group may reuse the previous step's sets while its
+// queries stay within cosine tau of the previous ones; one set may be
+// shared by a group (chosen on the summed keys); the index statistics may be
+// read as bf16 (two tiles per stage).
 #include <float.h>
 #include <limits.h>
 #include <stddef.h>
@@ -1881,36 +1893,36 @@ __device__ __forceinline__ void vsum_tiles(const DecodeArgs& a, DecSmem& S, Ring
         continue;
       }
       for (int sub = 0; sub < nsub; ++sub, ++i) {  // the tiles of the stage (one group)
-      const int c0 = (j * a.Q + i - bg * a.tpg) * kTile;
-      const int nrows = min(kTile, a.C - c0);
-      float4 v[4];
+        const int c0 = (j * a.Q + i - bg * a.tpg) * kTile;
+        const int nrows = min(kTile, a.C - c0);
+        float4 v[4];
 #pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) {
-        const int row = warp * 4 + r4;
-        if (H16) {
-          const uint16_t* vs = reinterpret_cast<const uint16_t*>(S.ring[stage]) + sub * kTile * kD;
-          v[r4] = row < nrows ? bf4(lds2(vs + row * kD + lane * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          const float* vs = reinterpret_cast<const float*>(S.ring[stage]);
-          v[r4] = row < nrows ? lds4(vs + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const int row = warp * 4 + r4;
+          if (H16) {
+            const uint16_t* vs = reinterpret_cast<const uint16_t*>(S.ring[stage]) + sub * kTile * kD;
+            v[r4] = row < nrows ? bf4(lds2(vs + row * kD + lane * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            const float* vs = reinterpret_cast<const float*>(S.ring[stage]);
+            v[r4] = row < nrows ? lds4(vs + row * kD + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-      }
-      if (sub == nsub - 1) release(S, rg, stage);
-      const float s = lane < L4 ? S.a.chunk.sc[i][warp][lane] : -INFINITY;
-      const int nn = lane < L4 ? S.a.chunk.n[i][warp][jr] : 0;
-      const float p = (s > -INFINITY && nn > 0) ? exp2f(s * kLog2e - mL) : 0.f;
-      lacc += p * (float)nn;
+        if (sub == nsub - 1) release(S, rg, stage);
+        const float s = lane < L4 ? S.a.chunk.sc[i][warp][lane] : -INFINITY;
+        const int nn = lane < L4 ? S.a.chunk.n[i][warp][jr] : 0;
+        const float p = (s > -INFINITY && nn > 0) ? exp2f(s * kLog2e - mL) : 0.f;
+        lacc += p * (float)nn;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pj = __shfl_sync(kFull, p, jj * G + h);
-          o[h].x += pj * v[jj].x;
-          o[h].y += pj * v[jj].y;
-          o[h].z += pj * v[jj].z;
-          o[h].w += pj * v[jj].w;
+          for (int h = 0; h < G; ++h) {
+            const float pj = __shfl_sync(kFull, p, jj * G + h);
+            o[h].x += pj * v[jj].x;
+            o[h].y += pj * v[jj].y;
+            o[h].z += pj * v[jj].z;
+            o[h].w += pj * v[jj].w;
+          }
         }
-      }
       }
     }
     // est partial slot of (chunk j, group bg): (j + bg) * G + h
