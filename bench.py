@@ -476,7 +476,7 @@ def measure_workload(w, r, dev, args, pk, flush, rank=0, want_cpu=False, label=N
         "bytes": by,
         "e2e": {"value": w.B / (e2e_mean * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": dstep.h2d_bytes, "d2h_bytes_per_step": dstep.d2h_bytes,
-                "ms_per_step": e2e_mean},
+                "ms_per_step": e2e_mean, "ms_per_step_median": statistics.median(e2e_ms)},
         "clocks": clocks, "gpu_launches": args.steps, "wall_s_timed": wall,
         "setup_seconds": {"generate": t_gen},
     }

@@ -255,8 +255,11 @@ class Decoder:
         self.layout = lay
         dev = index.device
         self.workspace = torch.zeros(lay.total, dtype=torch.uint8, device=dev)
-        self.out = torch.empty((c.B, Hq, c.d), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((c.B, Hq), dtype=torch.float32, device=dev)
+        # out and lse share one buffer, so one copy moves both to the host
+        n_out = c.B * Hq * c.d
+        self.results = torch.empty(n_out + c.B * Hq, dtype=torch.float32, device=dev)
+        self.out = self.results[:n_out].view(c.B, Hq, c.d)
+        self.lse = self.results[n_out:].view(c.B, Hq)
         self.topk = torch.empty((c.B, Hq, max(r, 1)), dtype=torch.int32, device=dev)
         self.reused = torch.zeros((c.B, Hq), dtype=torch.int32, device=dev)
 
@@ -384,8 +387,10 @@ class DecodeStep:
         dev = dec.index.device
         self.dec = dec
         self.q_host = torch.zeros((c.B, dec.Hq, c.d), dtype=torch.bfloat16, pin_memory=True)
-        self.out_host = torch.empty(tuple(dec.out.shape), dtype=torch.float32, pin_memory=True)
-        self.lse_host = torch.empty(tuple(dec.lse.shape), dtype=torch.float32, pin_memory=True)
+        self.results_host = torch.empty(dec.results.numel(), dtype=torch.float32, pin_memory=True)
+        n_out = dec.out.numel()
+        self.out_host = self.results_host[:n_out].view(tuple(dec.out.shape))
+        self.lse_host = self.results_host[n_out:].view(tuple(dec.lse.shape))
         self.q_dev = torch.zeros((c.B, dec.Hq, c.d), dtype=torch.bfloat16, device=dev)
         self.h2d_bytes = self.q_host.numel() * 2
         self.d2h_bytes = self.out_host.numel() * 4 + self.lse_host.numel() * 4
@@ -393,8 +398,7 @@ class DecodeStep:
         def body():
             self.q_dev.copy_(self.q_host, non_blocking=True)
             dec(self.q_dev, K, V, with_topk=False)
-            self.out_host.copy_(dec.out, non_blocking=True)
-            self.lse_host.copy_(dec.lse, non_blocking=True)
+            self.results_host.copy_(dec.results, non_blocking=True)
 
         self.graph = capture_graph(body, dev)
 
