@@ -203,7 +203,7 @@ int decode_layout(const wi_decode_params* p, int C, wi_decode_layout* L) {
   const size_t tph = (size_t)(p->sink + p->window + wi::kDecodeTile - 1) / wi::kDecodeTile;
   size_t off = kStatusBytes;
   L->counters = off;
-  L->counter_bytes = (int)align256(kSyncBytes + (groups + heads) * 4);
+  L->counter_bytes = (int)align256(kSyncBytes + (groups + 2 * heads) * 4);
   off += (size_t)L->counter_bytes;
   L->scores = off;
   off += align256(heads * (size_t)C * 4);
@@ -337,7 +337,8 @@ int fill_decode_args(const wi_decode_params* p, const void* q, const void* K, co
     a->sel_done = c + 1;
     a->grp_cnt = c + kSyncBytes / 4;
     a->head_cnt = a->grp_cnt + groups;
-    a->counter_words = (int)(groups + heads);
+    a->sel_flag = a->head_cnt + heads;
+    a->counter_words = (int)(groups + 2 * heads);
   }
   a->scores = reinterpret_cast<float*>(w + L.scores);
   a->head_max = reinterpret_cast<float*>(w + L.head_max);
@@ -434,6 +435,14 @@ int run_decode(const wi_decode_params* p, const void* q, const void* K, const vo
   a.lse = lse;
   a.topk_out = topk_ids;
   if (stages & wi::kStageAttend) a.inject = g_inject.exchange(0);
+  // few heads with short retrieval lists (about r N_idx / C <= 4096 tokens a
+  // head): each head's retrieval on its own block range, started as soon as
+  // that head is selected (no wait for every selection, no partition).  With
+  // longer lists the token-balanced split over all heads wins.  The stage
+  // calls split the same way, so they compose to the fused call.
+  const long long est_tokens = a.C > 0 ? (long long)a.r * a.N_idx / a.C : 0;
+  a.ret_per_head = (!a.share && a.r > 0 && (long long)a.B * a.Hq * 4 <= a.nb &&
+                    est_tokens <= 4096) ? 1 : 0;
   return cuda_status(wi::launch_decode(a, (cudaStream_t)stream));
 }
 

@@ -1408,8 +1408,122 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
   inject = __shfl_sync(kFull, (int)inject, 0) != 0;
   if (*(volatile int*)&S.abort || !(a.stages & kStageAttend)) return;
 
+  // retrieval tiles of tokens [x0, x1) of head bh (its clusters in id
+  // order, 64 tokens per tile); false once this block aborted
+  auto stream_piece = [&](int bh, int x0, int x1) -> bool {
+    const int rs = a.r;
+    const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
+    const size_t head = (size_t)b * a.Hkv + g;
+    const uint16_t* Ks = a.ksorted + head * (size_t)a.N_idx * kD;
+    const uint16_t* Vs = a.vsorted + head * (size_t)a.N_idx * kD;
+    const int* rows_g = a.sel_rows + (size_t)bh * rs;
+    const int* cnts_g = a.sel_cnts + (size_t)bh * rs;
+    const int* pre_g = a.sel_pre + (size_t)bh * rs;
+    const float* ss_g = a.sel_sc + (size_t)bh * rs;
+    // first cluster: the last j with pre_j <= x0 (32-ary search)
+    int jlo = 0, jhi = rs;  // answer in [jlo, jhi)
+    while (jhi - jlo > 1) {
+      const int step = (jhi - jlo + 31) / 32;
+      const int jj = jlo + lane * step;
+      const int pj = jj < jhi ? __ldcg(pre_g + jj) : INT_MAX;
+      const unsigned le = __ballot_sync(kFull, jj < jhi && pj <= x0);
+      const int k = 31 - __clz(le);  // lanes 0..k hold pre <= x0 (pre ascending)
+      jlo = jlo + k * step;
+      jhi = min(jhi, jlo + step);
+    }
+    // clusters in two windows of 32 (A current, B prefetched): lane i of a
+    // window holds cluster jA + i (or jA + 32 + i): first sorted row,
+    // count, first token (piece-relative to the head) and score
+    int jA = jlo;
+    auto load_win = [&](int jbase, int& row, int& cnt, int& st, float& s2) {
+      const int j = jbase + lane;
+      row = 0;
+      cnt = 0;
+      st = INT_MAX;
+      s2 = 0.f;
+      if (j < rs) {
+        row = __ldcg(rows_g + j);
+        cnt = __ldcg(cnts_g + j);
+        st = __ldcg(pre_g + j);
+        s2 = __ldcg(ss_g + j) * kLog2e;
+        if (cnt < 0 || row < 0 || (long long)row + cnt > a.N_idx) {
+          report(a.status, WI_ERR_INDEX_MISMATCH);
+          cnt = 0;
+          row = 0;
+        }
+      }
+    };
+    int rowA, cntA, stA, rowB, cntB, stB;
+    float sA, sB;
+    load_win(jA, rowA, cntA, stA, sA);
+    load_win(jA + 32, rowB, cntB, stB, sB);
+    auto shift = [&]() {  // A <- B, B <- the next 32 clusters
+      rowA = rowB;
+      cntA = cntB;
+      stA = stB;
+      sA = sB;
+      jA += 32;
+      load_win(jA + 32, rowB, cntB, stB, sB);
+    };
+    // end (exclusive) of window A's last cluster
+    auto endA = [&]() {
+      const int st = __shfl_sync(kFull, stA, 31), cnt = __shfl_sync(kFull, cntA, 31);
+      return st == INT_MAX ? INT_MAX : st + cnt;
+    };
+    for (int x = x0; x < x1; x += kTile) {
+      const int e = min(x + kTile, x1), n = e - x;
+      while (endA() <= x && jA + 32 < rs) shift();  // A fully used before this tile
+      int stage;
+      if (!slot(stage)) return false;
+      // every cluster meeting [x, e): the score of its token slots (side
+      // data) and the copies of its K and V rows
+      uint32_t bytes = 0;
+      for (;;) {
+        const int y0 = max(x, stA), y1 = min(e, stA == INT_MAX ? stA : stA + cntA);
+        if (y0 < y1) {
+          for (int y = y0; y < y1; ++y) S.side[stage].s[y - x] = sA;
+          const size_t srow = (size_t)rowA + (y0 - stA);
+          const uint32_t d = (uint32_t)(y0 - x) * 256u, nb2 = (uint32_t)(y1 - y0) * 256u;
+          copy_to(S.ring[stage] + d, Ks + srow * kD, nb2, stage);
+          copy_to(S.ring[stage] + kStageBytes / 2 + d, Vs + srow * kD, nb2, stage);
+          bytes += 2u * nb2;
+        }
+        if (endA() >= e || jA + 32 >= rs) break;
+        shift();  // the tile runs past window A
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFull, bytes, o);
+      if (lane == 0) {
+        TileInfo ti;
+        ti.kind = kTileRet;
+        ti.bh = bh;
+        ti.ntok = n;
+        ti.last = (e == x1);
+        S.info[stage] = ti;
+        copy_to(S.qs[stage], a.q + (size_t)bh * kD, kD * 2, stage);
+      }
+      post(stage, bytes + kD * 2u);
+      commit();
+    }
+    return true;
+  };
   // 3. retrieval tiles of the block's share of the retrieved tokens
-  if (a.r > 0) {
+  if (a.r > 0 && a.ret_per_head) {
+    // part p of P of one head: its tokens [T p / P, T (p + 1) / P), once that
+    // head's selection is published
+    const int bh = (int)(((long long)blockIdx.x * H) / a.nb);
+    const int b0 = ret_first(a, bh), P = ret_first(a, bh + 1) - b0;
+    int good = 1;
+    if (lane == 0 && a.fused) {
+      good = !*(volatile int*)&S.abort && count_wait(a.sel_flag + bh, 1u, a.status, &S.abort);
+      if (!good) *(volatile int*)&S.abort = 1;
+    }
+    if (!__shfl_sync(kFull, good, 0)) return;
+    __syncwarp();
+    const long long T = __ldcg(a.head_tok + bh), p = (long long)blockIdx.x - b0;
+    const int x0 = (int)(T * p / P), x1 = (int)(T * (p + 1) / P);
+    if (x0 < x1 && !stream_piece(bh, x0, x1)) return;
+  } else if (a.r > 0) {
     if (a.fused) {
       int good = 1;
       if (lane == 0) {
@@ -1430,7 +1544,6 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
     }
     partition(a, S, Ttot);
     const long long t0 = S.bnd[blockIdx.x], t1 = S.bnd[blockIdx.x + 1];
-    const int rs = a.r;
     // walk the heads that meet [t0, t1)
     long long P = 0;  // first token of the current head window
     for (long long h0 = 0; h0 < H && P < t1; h0 += 32) {
@@ -1450,100 +1563,7 @@ __device__ void producer(const DecodeArgs& a, DecSmem& S) {
         const long long hlo = __shfl_sync(kFull, lo_l, src);
         const int Th = __shfl_sync(kFull, th, src);
         const int x0 = (int)max(0ll, t0 - hlo), x1 = (int)min((long long)Th, t1 - hlo);
-        // the piece: tokens [x0, x1) of head bh
-        const int b = bh / a.Hq, g = (bh - b * a.Hq) / G;
-        const size_t head = (size_t)b * a.Hkv + g;
-        const uint16_t* Ks = a.ksorted + head * (size_t)a.N_idx * kD;
-        const uint16_t* Vs = a.vsorted + head * (size_t)a.N_idx * kD;
-        const int* rows_g = a.sel_rows + (size_t)bh * rs;
-        const int* cnts_g = a.sel_cnts + (size_t)bh * rs;
-        const int* pre_g = a.sel_pre + (size_t)bh * rs;
-        const float* ss_g = a.sel_sc + (size_t)bh * rs;
-        // first cluster: the last j with pre_j <= x0 (32-ary search)
-        int jlo = 0, jhi = rs;  // answer in [jlo, jhi)
-        while (jhi - jlo > 1) {
-          const int step = (jhi - jlo + 31) / 32;
-          const int jj = jlo + lane * step;
-          const int pj = jj < jhi ? __ldcg(pre_g + jj) : INT_MAX;
-          const unsigned le = __ballot_sync(kFull, jj < jhi && pj <= x0);
-          const int k = 31 - __clz(le);  // lanes 0..k hold pre <= x0 (pre ascending)
-          jlo = jlo + k * step;
-          jhi = min(jhi, jlo + step);
-        }
-        // clusters in two windows of 32 (A current, B prefetched): lane i of a
-        // window holds cluster jA + i (or jA + 32 + i): first sorted row,
-        // count, first token (piece-relative to the head) and score
-        int jA = jlo;
-        auto load_win = [&](int jbase, int& row, int& cnt, int& st, float& s2) {
-          const int j = jbase + lane;
-          row = 0;
-          cnt = 0;
-          st = INT_MAX;
-          s2 = 0.f;
-          if (j < rs) {
-            row = __ldcg(rows_g + j);
-            cnt = __ldcg(cnts_g + j);
-            st = __ldcg(pre_g + j);
-            s2 = __ldcg(ss_g + j) * kLog2e;
-            if (cnt < 0 || row < 0 || (long long)row + cnt > a.N_idx) {
-              report(a.status, WI_ERR_INDEX_MISMATCH);
-              cnt = 0;
-              row = 0;
-            }
-          }
-        };
-        int rowA, cntA, stA, rowB, cntB, stB;
-        float sA, sB;
-        load_win(jA, rowA, cntA, stA, sA);
-        load_win(jA + 32, rowB, cntB, stB, sB);
-        auto shift = [&]() {  // A <- B, B <- the next 32 clusters
-          rowA = rowB;
-          cntA = cntB;
-          stA = stB;
-          sA = sB;
-          jA += 32;
-          load_win(jA + 32, rowB, cntB, stB, sB);
-        };
-        // end (exclusive) of window A's last cluster
-        auto endA = [&]() {
-          const int st = __shfl_sync(kFull, stA, 31), cnt = __shfl_sync(kFull, cntA, 31);
-          return st == INT_MAX ? INT_MAX : st + cnt;
-        };
-        for (int x = x0; x < x1; x += kTile) {
-          const int e = min(x + kTile, x1), n = e - x;
-          while (endA() <= x && jA + 32 < rs) shift();  // A fully used before this tile
-          int stage;
-          if (!slot(stage)) return;
-          // every cluster meeting [x, e): the score of its token slots (side
-          // data) and the copies of its K and V rows
-          uint32_t bytes = 0;
-          for (;;) {
-            const int y0 = max(x, stA), y1 = min(e, stA == INT_MAX ? stA : stA + cntA);
-            if (y0 < y1) {
-              for (int y = y0; y < y1; ++y) S.side[stage].s[y - x] = sA;
-              const size_t srow = (size_t)rowA + (y0 - stA);
-              const uint32_t d = (uint32_t)(y0 - x) * 256u, nb2 = (uint32_t)(y1 - y0) * 256u;
-              copy_to(S.ring[stage] + d, Ks + srow * kD, nb2, stage);
-              copy_to(S.ring[stage] + kStageBytes / 2 + d, Vs + srow * kD, nb2, stage);
-              bytes += 2u * nb2;
-            }
-            if (endA() >= e || jA + 32 >= rs) break;
-            shift();  // the tile runs past window A
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(kFull, bytes, o);
-          if (lane == 0) {
-            TileInfo ti;
-            ti.kind = kTileRet;
-            ti.bh = bh;
-            ti.ntok = n;
-            ti.last = (e == x1);
-            S.info[stage] = ti;
-            copy_to(S.qs[stage], a.q + (size_t)bh * kD, kD * 2, stage);
-          }
-          post(stage, bytes + kD * 2u);
-          commit();
-        }
+        if (!stream_piece(bh, x0, x1)) return;
       }
       P += __shfl_sync(kFull, incl, 31);
     }
@@ -1829,7 +1849,10 @@ __device__ __forceinline__ void selections(const DecodeArgs& a, DecSmem& S, cons
       const bool ok = a.fused ? wait_count_all(a, S, a.grp_cnt + bg, (unsigned)a.tpg) : !cany(rg.hollow);
       if (!ok) continue;
       select_head(a, S, bh);
-      if (a.fused && tid == 0) publish(S, a, a.sel_done, a.share ? (unsigned)G : 1u, 1);
+      if (a.fused && tid == 0) {
+        publish(S, a, a.sel_done, a.share ? (unsigned)G : 1u, 1);
+        if (a.ret_per_head) publish(S, a, a.sel_flag + bh, 1u, 1);
+      }
     }
   }
 }
@@ -2133,6 +2156,9 @@ __device__ __forceinline__ void merges(const DecodeArgs& a, DecSmem& S) {
   const int H = a.B * a.Hq;
   for (int bh = blk; bh < H; bh += a.nb) {
     const int bg = bh / a.G;
+    // with per-head ranges this block need not have waited for the head's
+    // selection: its token count is read only once it is published
+    if (a.ret_per_head && a.fused && !wait_count_all(a, S, a.sel_flag + bh, 1u)) break;
     // this head's retrieval pieces: blocks whose share meets its tokens
     int P_lo = 0;
     {
@@ -2145,13 +2171,19 @@ __device__ __forceinline__ void merges(const DecodeArgs& a, DecSmem& S) {
       csync();
     }
     const int Th = a.r > 0 ? __ldcg(a.head_tok + bh) : 0;
-    // blocks whose share is non-empty and meets [P_lo, P_lo + Th), in order
+    // blocks whose share is non-empty and meets [P_lo, P_lo + Th), in order;
+    // with per-head ranges, the blocks of the head's range with a non-empty part
     if (tid == 0) {
       int n = 0;
-      if (Th > 0)
+      if (Th > 0 && a.ret_per_head) {
+        const int b0 = ret_first(a, bh), P = ret_first(a, bh + 1) - b0;
+        for (int p = 0; p < P; ++p)
+          if ((long long)Th * (p + 1) / P > (long long)Th * p / P) S.u.merge.rb[n++] = b0 + p;
+      } else if (Th > 0) {
         for (int b = 0; b < a.nb; ++b)
           if (S.bnd[b] < S.bnd[b + 1] && S.bnd[b + 1] > P_lo && S.bnd[b] < P_lo + Th)
             S.u.merge.rb[n++] = b;
+      }
       S.u.merge.cnt[0] = n;
     }
     csync();
@@ -2216,6 +2248,10 @@ __device__ void consumers(const DecodeArgs& a, DecSmem& S) {
   }
   if (a.stages & kStageAttend) {
     steady_tiles<G>(a, S, rg);  // 2.
+    // the retrieval pieces' per-warp states share shared memory with the
+    // value-sum tiles' scores: no warp may start on them while another still
+    // reads those scores
+    csync();
     retrieval_tiles(a, S, rg);  // 3.
   }
   // 4. merges

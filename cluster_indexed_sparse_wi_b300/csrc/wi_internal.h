@@ -74,7 +74,8 @@ struct DecodeArgs {
   unsigned* sel_done;   // heads whose selection is published
   unsigned* grp_cnt;    // [B*Hkv] index tiles scored per KV group
   unsigned* head_cnt;   // [B*Hq]  partials published per query head
-  int counter_words;    // words from grp_cnt to the end of head_cnt (contiguous)
+  unsigned* sel_flag;   // [B*Hq]  the head's selection is published
+  int counter_words;    // words from grp_cnt to the end of sel_flag (contiguous)
   float* scores;        // [B,Hq,C]   s_c (f32), -inf for empty clusters
   float* head_max;      // [B,Hq]
   int* sel_ids;         // [B,Hq,rs]  retrieved ids ascending, -1 padding (rs = max(r,1))
@@ -98,6 +99,8 @@ struct DecodeArgs {
   int nchunks;          // ceil(nt / Q); chunk j is taken by block j % nb in round j / nb
   int rounds;           // ceil(nchunks / nb)
   int kbar_first;       // every round's centroid-key tiles before any selection
+  int ret_per_head;     // retrieval by fixed per-head block ranges (few heads), each
+                        // started once its head's selection is published
   int inject;           // test hook: every block skips the copies of its first tile
   // selection options
   int rank_mass;        // rank clusters by s_c + ln n_c instead of s_c
@@ -141,6 +144,12 @@ __host__ __device__ inline int sel_round(const DecodeArgs& a, int bh) {
 // Steady tile t (of B*Hkv*tph) is taken by block nb - 1 - t % nb.
 __host__ __device__ inline int steady_block(const DecodeArgs& a, int t) {
   return a.nb - 1 - t % a.nb;
+}
+// With a.ret_per_head, head bh's retrieved tokens are split evenly over the
+// blocks [ret_first(bh), ret_first(bh + 1)).
+__host__ __device__ inline int ret_first(const DecodeArgs& a, int bh) {
+  const int H = a.B * a.Hq;
+  return (int)(((long long)bh * a.nb + H - 1) / H);
 }
 // Head bh is merged by block bh % nb.
 __host__ __device__ inline int merge_block(const DecodeArgs& a, int bh) { return bh % a.nb; }

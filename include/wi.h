@@ -211,9 +211,10 @@ WI_API size_t wi_decode_workspace_bytes(const wi_decode_params *p, int n_cluster
 typedef struct {
   size_t counters;      /* per-call progress counters: launch-wide words
                            (blocks finished, selections published; 256 B),
-                           then u32 [B*Hkv] scored index tiles and u32 [B*Hq]
-                           published partials; zero before the first call;
-                           every call leaves them at zero                  */
+                           then u32 [B*Hkv] scored index tiles, u32 [B*Hq]
+                           published partials and u32 [B*Hq] published
+                           selections; zero before the first call; every
+                           call leaves them at zero                        */
   size_t scores;        /* f32 [B,Hq,C]   s_c = scale q.kbar_c, -inf if empty */
   size_t head_max;      /* f32 [B,Hq]     max_c s_c                           */
   size_t selected;      /* i32 [B,Hq,max(r,1)]  retrieved ids ascending, -1 pad */
