@@ -229,6 +229,20 @@ def test_segments_hand_case():
     assert [list(x) for x in segs] == [list(range(20))]
 
 
+def test_steady_zone_and_segments_partition_the_sequence():
+    # every position is in exactly one of: the steady zone (first `sink`, last
+    # `window`) or one segment, and a segment only holds its own span
+    for N, sink, window, L in [(20, 3, 4, 8), (37, 0, 5, 16), (37, 4, 0, 16), (64, 4, 60, 16),
+                               (50, 0, 0, 7), (9, 2, 7, 4)]:
+        st = wi.steady_positions(N, sink, window)
+        assert st.tolist() == [p for p in range(N) if p < sink or p >= N - window]
+        segs = wi.segment_positions(N, sink, window, L)
+        assert len(segs) == -(-N // L)
+        for s, ps in enumerate(segs):
+            assert all(s * L <= p < (s + 1) * L for p in ps)
+        assert sorted(st.tolist() + [int(p) for ps in segs for p in ps]) == list(range(N))
+
+
 def test_init_strided_hand_case():
     # m = 10 keys along distinct axes; k = 4 picks floor(j*10/4) = 0, 2, 5, 7
     keys = np.eye(10) * 3.0
@@ -334,6 +348,38 @@ def test_statistics_invariants_and_stable_order():
     for p in P:
         assert idx["assign"][p] // 10 == p // 200
     assert np.all(idx["assign"][:4] == -1) and np.all(idx["assign"][N - 32:] == -1)
+
+
+def test_index_statistics_bruteforce_loops_and_empty_cluster():
+    # sizes, offsets, member order, mean keys and value sums of a hand-made
+    # assignment, by Python loops; cluster 2 is left empty
+    rng = np.random.default_rng(31)
+    N, d, C = 40, 6, 5
+    K = rng.standard_normal((N, d))
+    V = rng.standard_normal((N, d))
+    pos = np.arange(3, 37)
+    c = rng.integers(0, C, pos.size)
+    c[c == 2] = 4
+    st = wi.index_statistics(K, V, pos, c, C)
+    before = 0
+    for j in range(C):
+        mem = [int(p) for p, cj in zip(pos, c) if cj == j]
+        assert st["size"][j] == len(mem)
+        assert st["offset"][j] == before
+        assert st["perm"][before:before + len(mem)].tolist() == sorted(mem)
+        before += len(mem)
+        ks, vs = [0.0] * d, [0.0] * d
+        for p in mem:
+            for e in range(d):
+                ks[e] += K[p, e]
+                vs[e] += V[p, e]
+        kbar = [x / len(mem) for x in ks] if mem else [0.0] * d
+        np.testing.assert_allclose(st["centroid_key"][j], kbar, rtol=2.0 ** -23, atol=1e-12)
+        np.testing.assert_allclose(st["value_sum"][j], vs, rtol=2.0 ** -23, atol=1e-12)
+    assert st["offset"][C] == pos.size
+    assert np.all(st["centroid_key"][2] == 0) and np.all(st["value_sum"][2] == 0)
+    np.testing.assert_array_equal(st["k_sorted"], K[st["perm"]])
+    np.testing.assert_array_equal(st["v_sorted"], V[st["perm"]])
 
 
 # ---------------------------------------------------------------- format and GQA wrapper
